@@ -1,0 +1,407 @@
+#!/usr/bin/env python
+"""Benchmark of the quantized MoE expert layer on GB300.
+
+One step = one full pass of the layer (router + top-k, counting sort + permute, FC1 with
+fused dequant and activation, FC2, shared expert, un-permute/combine) over one batch of T
+synthetic tokens; for a stacked config (Phi-shaped, 32 layers) one step runs every layer.
+
+Default workload: the encoder-decoder MoE FFN (d=1024, ffn=4096, E=32, top-1, GELU,
+INT4 per-channel, fp16 activations) at T = 3840 tokens (40-token sentences x batch 96).
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle instead, on a
+bounded token sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from weight_only_int4_route_gb300 import synth  # noqa: E402
+
+METRIC = "MoE-layer tokens/s at 1 GB300; % of HBM (decode) / tensor (prefill) roofline"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="encdec_int4", choices=sorted(synth.CONFIGS))
+    ap.add_argument("--T", type=int, default=0, help="tokens per step (default: the config's largest)")
+    ap.add_argument("--layers", type=int, default=0, help="stacked layers per step (default: the config's)")
+    ap.add_argument("--cpu-sample", type=int, default=256, help="tokens in the oracle's timed sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+# ---------------------------------------------------------------- algorithmic work
+
+
+def packed_bytes(K, N, bits, group):
+    G = 1 if group == 0 else K // group
+    return K * N * bits // 8 + G * N * 2
+
+
+def work_model(cfg, T, counts):
+    """Algorithmic bytes and FLOPs of one layer and of its two grouped GEMM launches.
+
+    Weights are counted once per active expert (experts with no routed rows load none);
+    FC1 reads Xp (R x d) and writes H (R x F) in 16-bit; FC2 reads H and writes fp32 Yp."""
+    R = T * cfg.k
+    act_e = sum(1 for c in counts if c > 0)
+    w1 = packed_bytes(cfg.d, cfg.F1, cfg.bits, cfg.group)
+    w2 = packed_bytes(cfg.F, cfg.d, cfg.bits, cfg.group)
+    fc1 = dict(bytes=act_e * w1 + R * cfg.d * 2 + R * cfg.F * 2, flops=2 * R * cfg.d * cfg.F1)
+    fc2 = dict(bytes=act_e * w2 + R * cfg.F * 2 + R * cfg.d * 4, flops=2 * R * cfg.F * cfg.d)
+    sh_w = 3 * cfg.d * cfg.Fs * 2
+    router_w = cfg.d * cfg.E * (4 if cfg.router_dtype == "f32" else 2)
+    layer = dict(bytes=act_e * (w1 + w2) + sh_w + router_w + 2 * T * cfg.d * 2,
+                 flops=2 * R * (cfg.d * cfg.F1 + cfg.F * cfg.d) + 2 * T * 3 * cfg.d * cfg.Fs + 2 * T * cfg.d * cfg.E)
+    return dict(fc1=fc1, fc2=fc2, layer=layer, active_experts=act_e)
+
+
+# ---------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- our arm
+
+
+def run_ours(args, cfg, T, n_layers, world, rank, local):
+    from weight_only_int4_route_gb300 import build as B
+    from weight_only_int4_route_gb300 import moe as M
+
+    B.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    # ---- weights: distinct layers for a stack; else rotate copies so the step's weight
+    # stream never fits in L2 (inputs larger than L2 between timed iterations)
+    est_touch = None
+    w0 = synth.layer_weights(cfg, 0, device=dev)
+    packed = [M.PackedLayer.from_weights(cfg, w0, dev)]
+    per_layer = sum(t.numel() for t in (packed[0].w1, packed[0].w2)) + sum(
+        t.numel() * t.element_size() for t in (packed[0].ws_gu, packed[0].ws_d) if t is not None)
+    del w0
+    if n_layers > 1:
+        copies = n_layers
+    else:
+        # bytes one step touches: active experts' weights + shared + activations
+        R = T * cfg.k
+        act_e = min(cfg.E, R)
+        act_e = cfg.E * (1 - (1 - min(1.0, cfg.k / cfg.E)) ** T) if act_e < cfg.E else cfg.E
+        est_touch = act_e * (packed_bytes(cfg.d, cfg.F1, cfg.bits, cfg.group) + packed_bytes(cfg.F, cfg.d, cfg.bits, cfg.group)) \
+            + 3 * cfg.d * cfg.Fs * 2 + T * cfg.d * 2 * 4
+        copies = max(2, math.ceil(3 * L2_BYTES / max(est_touch, 1)))
+        copies = min(copies, 16)
+    for i in range(1, copies):
+        wi = synth.layer_weights(cfg, i, device=dev)
+        packed.append(M.PackedLayer.from_weights(cfg, wi, dev))
+        del wi
+    nx = copies if n_layers == 1 else 1
+    xs = [synth.normal(cfg, "x", (T, cfg.d), 1.0, cfg.torch_dtype, layer=i, extra=T, device=dev) for i in range(nx)]
+    outs = [torch.empty((T, cfg.d), dtype=cfg.torch_dtype, device=dev) for _ in range(max(1, n_layers if n_layers > 1 else 1))]
+    ws_bytes = M.Layer(packed[0], T).ws_bytes
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    layers = [M.Layer(p, T, workspace=ws) for p in packed]
+    torch.cuda.synchronize()
+
+    def step(i):
+        if n_layers > 1:
+            for li, layer in enumerate(layers):
+                layer.forward(xs[0], outs[li])
+        else:
+            j = i % copies
+            layers[j].forward(xs[j % nx], outs[0])
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    for i in range(args.warmup):
+        step(i)
+    barrier()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    t1.record()
+    barrier()
+    elapsed_ms = t0.elapsed_time(t1)
+
+    # ---- per-stage durations inside the same workload (roofline of the dominant kernel)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in M.STAGES] for _ in range(len(layers))]
+    for ring in evs:
+        for e in ring:
+            e.record()
+    torch.cuda.synchronize()
+    stage_ms = {s: 0.0 for s in M.STAGES[1:]}
+    n_prof = 0
+    for i in range(args.steps):
+        if n_layers > 1:
+            for li, layer in enumerate(layers):
+                layer.forward_profiled(xs[0], outs[li], evs[li])
+            torch.cuda.synchronize()
+            for li in range(len(layers)):
+                for a, b, s in zip(evs[li][:-1], evs[li][1:], M.STAGES[1:]):
+                    stage_ms[s] += a.elapsed_time(b)
+                n_prof += 1
+        else:
+            j = i % copies
+            layers[j].forward_profiled(xs[j % nx], outs[0], evs[0])
+            torch.cuda.synchronize()
+            for a, b, s in zip(evs[0][:-1], evs[0][1:], M.STAGES[1:]):
+                stage_ms[s] += a.elapsed_time(b)
+            n_prof += 1
+    stage_ms = {s: v / max(n_prof, 1) for s, v in stage_ms.items()}
+    clk = clocks.stop()
+
+    # ---- end to end through the public call with host buffers
+    e2e = None
+    if not args.no_e2e:
+        xh = xs[0].cpu().pin_memory()
+        oh = torch.empty((T, cfg.d), dtype=cfg.torch_dtype).pin_memory()
+        xd = torch.empty_like(xs[0])
+        ksteps = max(3, min(args.steps, 50))
+
+        def e2e_step(i):
+            xd.copy_(xh, non_blocking=True)
+            if n_layers > 1:
+                for li, layer in enumerate(layers):
+                    layer.forward(xd, outs[li])
+                oh.copy_(outs[-1], non_blocking=True)
+            else:
+                layers[i % copies].forward(xd, outs[0])
+                oh.copy_(outs[0], non_blocking=True)
+
+        for i in range(3):
+            e2e_step(i)
+        barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for i in range(ksteps):
+            e2e_step(i)
+        b.record()
+        barrier()
+        e2e_ms = a.elapsed_time(b) / ksteps
+        e2e = dict(ms=e2e_ms, h2d=T * cfg.d * 2, d2h=T * cfg.d * 2)
+
+    # routing counts of layer 0 for the algorithmic work
+    layers[0].forward(xs[0], outs[0])
+    torch.cuda.synchronize()
+    offs = layers[0].routing(T)["offsets"].cpu().tolist()
+    counts = [offs[i + 1] - offs[i] for i in range(cfg.E)]
+    launches_per_layer = layers[0].launch_count(T)
+
+    ms_local = elapsed_ms / args.steps
+    ms = ms_local
+    if dist is not None:
+        t = torch.tensor([ms_local], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+        if e2e is not None:
+            t = torch.tensor([e2e["ms"]], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e["ms"] = float(t.item())
+    return dict(ms=ms, stage_ms=stage_ms, counts=counts, clocks=clk, e2e=e2e, copies=copies,
+                launches=launches_per_layer * n_layers * args.steps, per_layer_bytes=per_layer,
+                est_touch=est_touch, dist=dist)
+
+
+def cpu_baseline(cfg, T, sample, n_layers):
+    """Time the CPU oracle, as it stands, on a bounded token sample of the workload."""
+    from oracle import moe_oracle as O
+    w = synth.layer_weights(cfg, 0)
+    x = synth.activations(cfg, T)
+    sub = torch.randperm(T, generator=torch.Generator().manual_seed(T))[:min(sample, T)].sort().values
+    O.moe_layer(x[:8], w, cfg)     # warm the allocator
+    t = time.perf_counter()
+    O.moe_layer(x, w, cfg, token_subset=sub)
+    dt = time.perf_counter() - t
+    # one layer of a stack per sample: tokens/s of the whole stack = per-layer rate / layers
+    value = len(sub) / dt / n_layers
+    return {"value": value, "unit": "tokens/s", "cores": torch.get_num_threads(), "kind": "oracle",
+            "sample": f"float64 oracle: full routing of all {T} tokens, expert FFNs and combine for {len(sub)} "
+                      f"seeded tokens of layer 0" + (f", rate divided by {n_layers} layers" if n_layers > 1 else ""),
+            "seconds": dt}
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_env()
+    cfg = synth.CONFIGS[args.config]
+    T = args.T or max(cfg.T)
+    n_layers = args.layers or cfg.layers
+    workload = (f"{cfg.name}: d={cfg.d} ffn={cfg.F} E={cfg.E} top-{cfg.k} {cfg.act} INT{cfg.bits} "
+                f"{'per-channel' if cfg.group == 0 else 'group-128'} {cfg.dtype} activations"
+                + (f" + shared expert Fs={cfg.Fs}" if cfg.Fs else "") + (f", Zipf({cfg.zipf}) logit bias" if cfg.zipf else "")
+                + f", T={T} tokens" + (f", {n_layers} stacked layers" if n_layers > 1 else ""))
+    base_cfg = {"workload": workload, "config": cfg.name, "T": T, "layers": n_layers}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        from oracle import moe_oracle as O
+        w = synth.layer_weights(cfg, 0)
+        x = synth.activations(cfg, T)
+        sample = min(64, T)
+        gen = torch.Generator().manual_seed(7)
+        times = []
+        for i in range(args.warmup + args.steps):
+            sub = torch.randperm(T, generator=gen)[:sample].sort().values
+            t = time.perf_counter()
+            O.moe_layer(x, w, cfg, token_subset=sub)
+            if i >= args.warmup:
+                times.append(time.perf_counter() - t)
+        per_step = sum(times) / len(times)
+        value = sample / per_step / n_layers
+        cores = torch.get_num_threads()
+        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+                "config": dict(base_cfg, l2="CPU run"),
+                "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                 "sample": f"each step: float64 oracle routing all {T} tokens, expert FFNs + combine "
+                                           f"for {sample} seeded tokens of layer 0"},
+                "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    r = run_ours(args, cfg, T, n_layers, world, rank, local)
+    peaks, peak_src = load_peaks()
+    wm = work_model(cfg, T, r["counts"])
+    value = world * T / (r["ms"] * 1e-3)
+    # dominant kernel: the longer of the two grouped GEMM stages
+    st = r["stage_ms"]
+    dom = "fc1" if st["fc1"] >= st["fc2"] else "fc2"
+    dom_ms = st[dom]
+    work = wm[dom]
+    intensity = work["flops"] / work["bytes"]
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if intensity >= ridge:
+        peak = peaks["bf16_tflops_sustained"] if "bf16_tflops_sustained" in peaks else peaks["bf16_tflops"]
+        achieved = work["flops"] / (dom_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_source": f"{peak_src} bf16 sustained (kernel timed inside back-to-back steps)"}
+    else:
+        peak = peaks["hbm_gbs"]
+        achieved = work["bytes"] / (dom_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "peak_source": f"{peak_src} HBM copy bandwidth"}
+    roof.update({"traffic": None, "kernel": f"grouped GEMM {dom.upper()} (gemm_mma_kernel)",
+                 "algorithmic_bytes": work["bytes"], "algorithmic_flops": work["flops"], "ms_per_launch": dom_ms})
+    layer_ms = r["ms"] / n_layers
+    lw = wm["layer"]
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": r["ms"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
+            "config": dict(base_cfg, l2=(f"inputs larger than L2: {r['copies']} rotating weight/activation copies"
+                                         if n_layers == 1 else f"{n_layers} distinct layers per step"),
+                           active_experts=wm["active_experts"],
+                           layer_roofline={"hbm_frac": lw["bytes"] / (layer_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                                           "tensor_frac": lw["flops"] / (layer_ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                                           "bytes": lw["bytes"], "flops": lw["flops"]},
+                           stage_ms=st, parallelism=f"replicas x{world} (token data parallel)"),
+            "roofline": roof, "gpu_launches": r["launches"]}
+    if r["clocks"]:
+        line["clocks"] = r["clocks"]
+    if r["e2e"]:
+        e = r["e2e"]
+        line["e2e"] = {"value": world * T / (e["ms"] * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": e["h2d"],
+                       "d2h_bytes_per_step": e["d2h"]}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, T, args.cpu_sample, n_layers)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if r["dist"] is not None:
+        r["dist"].destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,78 @@
+"""CPU-only checks of the C ABI: the library loads, exports every symbol the header
+declares, and its host-side queries and argument validation answer without a GPU
+(no compute call is made here)."""
+import ctypes
+
+import pytest
+
+from weight_only_int4_route_gb300 import build as B
+from weight_only_int4_route_gb300 import moe as M
+
+
+@pytest.fixture(scope="module")
+def L():
+    B.build()
+    return M.lib()
+
+
+def test_every_header_symbol_is_exported(L):
+    names = M.header_symbols()
+    assert len(names) >= 19
+    missing = [n for n in names if not hasattr(L, n)]
+    assert missing == []
+    assert set(names) == set(M._SIGS), "binding and header disagree"
+
+
+def test_version_and_error_string(L):
+    assert L.moe_version() == 1
+    assert isinstance(L.moe_last_error_string(), bytes)
+
+
+def test_packed_sizes(L):
+    # INT4: E*N*K/2 bytes of words, then 256-aligned (E, G, N) 16-bit scales
+    assert L.moe_packed_scale_offset(2, 256, 64, 4) == 2 * 64 * 128
+    assert L.moe_packed_size(2, 256, 64, 4, 0) == 2 * 64 * 128 + 256
+    assert L.moe_packed_size(2, 256, 64, 4, 128) == 2 * 64 * 128 + 512
+    assert L.moe_packed_size(3, 256, 64, 8, 0) == 3 * 64 * 256 + 512
+    assert L.moe_packed_size(1, 256, 64, 16, 0) == 256 * 64 * 2
+    assert L.moe_packed_size(1, 100, 64, 4, 0) == 0          # K % 8 != 0
+    assert L.moe_packed_size(1, 256, 60, 4, 0) == 0          # N % 8 != 0
+    assert L.moe_packed_size(1, 192, 64, 4, 128) == 0        # K % 128 != 0 with group 128
+
+
+def test_permute_workspace_size(L):
+    assert L.moe_permute_workspace_size(16, 8, 2) == 2 * 256
+    assert L.moe_permute_workspace_size(4096, 60, 4) == 2 * ((64 * 60 * 4 + 255) // 256 * 256)
+
+
+def test_invalid_arguments_are_rejected_on_host(L):
+    nul = ctypes.c_void_p(0)
+    # bad bits
+    assert L.moe_pack_weights(nul, nul, 0, 1, 256, 64, 5, 0, nul, 0, nul) == -1
+    assert b"bits" in L.moe_last_error_string()
+    # bad dtype
+    assert L.moe_route_topk(nul, 7, nul, 0, nul, 4, 256, 8, 2, 0, nul, nul, nul) == -1
+    # k > E
+    assert L.moe_route_topk(nul, 0, nul, 0, nul, 4, 256, 8, 9, 0, nul, nul, nul) == -1
+    # T == 0 is a no-op
+    assert L.moe_route_topk(nul, 0, nul, 0, nul, 0, 256, 8, 2, 0, nul, nul, nul) == 0
+    # K not a multiple of 128
+    assert L.moe_grouped_gemm_w4a16(nul, 0, nul, 2, 200, 64, 0, nul, 4, 0, nul, 0, nul, 0, nul) == -1
+    # unsupported N
+    assert L.moe_grouped_gemm_w4a16(nul, 0, nul, 2, 256, 40, 0, nul, 4, 0, nul, 0, nul, 0, nul) == -2
+    # offsets NULL with E > 1
+    assert L.moe_grouped_gemm_w8a16(nul, 0, nul, 2, 256, 64, 0, nul, 4, 0, nul, 0, nul, 0, nul) == -1
+    # misaligned pointer
+    bad = ctypes.c_void_p(0x1003)
+    assert L.moe_unpermute_combine(bad, 2, bad, bad, nul, 2, 4, 64, 1, bad, 0, nul) == -1
+
+
+def test_layer_workspace_query(L):
+    from weight_only_int4_route_gb300 import synth
+    for name, cfg in synth.CONFIGS.items():
+        desc = M.layer_desc(cfg)
+        n = L.moe_layer_workspace_size(ctypes.byref(desc), max(cfg.T))
+        assert n > 0, name
+    bad = M.layer_desc(synth.CONFIGS["tiny"])
+    bad.k = 99
+    assert L.moe_layer_workspace_size(ctypes.byref(bad), 16) == 0

@@ -1,0 +1,317 @@
+"""GPU parity: every C-ABI call against the CPU oracle on the same seeded inputs.
+
+Bit-exact: packed words, dequantized weights, expert ids, offsets, permutations,
+gathered rows, and GEMMs whose products and partial sums are exact (integer inputs).
+Within tolerance: gates (fp32 vs float64) and layer outputs (rel L2 <= 5e-3,
+max-abs <= 2e-2 * max|ref|)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_oracle as O
+from weight_only_int4_route_gb300 import synth
+
+from _helpers import GATE_RTOL, assert_close_layer, have_gpu, layer_inputs
+
+pytestmark = [pytest.mark.gpu, pytest.mark.skipif(not have_gpu(), reason="needs a CUDA GPU")]
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def M():
+    from weight_only_int4_route_gb300 import build, moe
+    build.build()
+    moe.lib()
+    return moe
+
+
+def _codes(bits, shape, gen):
+    lo, hi = (-8, 8) if bits == 4 else (-128, 128)
+    return torch.randint(lo, hi, shape, generator=gen, dtype=torch.int8)
+
+
+def _scales(shape, dtype, gen):
+    return (torch.rand(shape, generator=gen) * 0.05 + 0.001).to(dtype)
+
+
+# ------------------------------------------------------------------ pack / dequant
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("group", [0, 128])
+def test_pack_words_match_oracle(M, bits, dtype, group):
+    gen = torch.Generator().manual_seed(100 + bits + group)
+    E, K, N = 3, 384, 136
+    q = _codes(bits, (E, K, N), gen)
+    s = _scales((E, 1 if group == 0 else K // 128, N), dtype, gen)
+    packed = M.pack_weights(q.to(DEV), s.to(DEV), bits, group).cpu()
+    ref_words = O.pack_int4(q.numpy()) if bits == 4 else O.pack_int8(q.numpy())
+    nbytes = ref_words.nbytes
+    got_words = packed[:nbytes].numpy().view(np.uint32).reshape(ref_words.shape)
+    assert np.array_equal(got_words, ref_words)
+    off = M.lib().moe_packed_scale_offset(E, K, N, bits)
+    assert torch.equal(packed[off:off + s.numel() * 2].view(dtype).view(s.shape), s)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("group", [0, 128])
+def test_dequant_bit_exact(M, bits, dtype, group):
+    gen = torch.Generator().manual_seed(200 + bits + group)
+    E, K, N = 2, 512, 264
+    q = _codes(bits, (E, K, N), gen)
+    s = _scales((E, 1 if group == 0 else K // 128, N), dtype, gen)
+    packed = M.pack_weights(q.to(DEV), s.to(DEV), bits, group)
+    for out_dt in (dtype, torch.float32):
+        got = M.dequant(packed, E, K, N, bits, group, dtype, out_dt).cpu()
+        ref = O.dequant_rounded(q, s, group, out_dt)
+        assert torch.equal(got.view(torch.int16 if out_dt != torch.float32 else torch.int32),
+                           ref.view(torch.int16 if out_dt != torch.float32 else torch.int32)), out_dt
+
+
+@pytest.mark.parametrize("name", ["encdec_int8", "encdec_int4", "qwen", "phi"])
+def test_dequant_config_shapes(M, name):
+    """Algorithm 1 bit-exact on each config's FC1 and FC2 shapes (one expert)."""
+    cfg = synth.CONFIGS[name]
+    for K, N in ((cfg.d, cfg.F1), (cfg.F, cfg.d)):
+        q = synth.codes(cfg, "q1", (1, K, N))
+        s = synth.scales(cfg, "s1", 1, K, N)
+        packed = M.pack_weights(q.to(DEV), s.to(DEV), cfg.bits, cfg.group)
+        got = M.dequant(packed, 1, K, N, cfg.bits, cfg.group, cfg.torch_dtype, cfg.torch_dtype).cpu()
+        ref = O.dequant_rounded(q, s, cfg.group, cfg.torch_dtype)
+        assert torch.equal(got.view(torch.int16), ref.view(torch.int16)), (name, K, N)
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+def test_i2f_every_code_every_slot(M, dtype):
+    """Every INT4 code in every nibble slot and every INT8 code in every byte decodes to itself."""
+    for bits, codes in ((4, range(-8, 8)), (8, range(-128, 128))):
+        per = 8 if bits == 4 else 4
+        vals = torch.tensor(list(codes), dtype=torch.int8)
+        K = 128 * ((len(vals) * per + 127) // 128)
+        q = torch.zeros((1, K, 8), dtype=torch.int8)
+        # run j, element i carries code vals[(j + i) % len]: every code visits every slot
+        for j in range(K // per):
+            for i in range(per):
+                q[0, j * per + i, :] = vals[(j + i) % len(vals)]
+        s = torch.ones((1, 1, 8), dtype=dtype)
+        packed = M.pack_weights(q.to(DEV), s.to(DEV), bits, 0)
+        got = M.dequant(packed, 1, K, 8, bits, 0, dtype, torch.float32).cpu()
+        assert torch.equal(got, q.to(torch.float32))
+
+
+# ------------------------------------------------------------------ router
+
+
+@pytest.mark.parametrize("name,T", [("tiny", 16), ("encdec_int4", 40), ("encdec_int4", 333), ("qwen", 32),
+                                    ("qwen", 4096), ("dsv2", 512), ("phi", 17)])
+def test_route_matches_oracle(M, name, T):
+    cfg = synth.CONFIGS[name]
+    w, x = layer_inputs(cfg, T)
+    bias = None if w.bias is None else w.bias.to(DEV)
+    ids, gate = M.route_topk(x.to(DEV), w.wr.to(DEV), bias, cfg.k)
+    lg, rids, rgate = O.route(x, w.wr, w.bias, cfg.k)
+    assert torch.equal(ids.cpu(), rids)
+    rel = ((gate.cpu().double() - rgate).abs() / rgate).max().item()
+    assert rel <= GATE_RTOL, rel
+
+
+def test_route_renormalize_and_max_experts(M):
+    cfg = synth.custom("qwen", d=256, E=256, k=8, router_dtype="bf16")
+    w, x = layer_inputs(cfg, 50)
+    ids, gate = M.route_topk(x.to(DEV), w.wr.to(DEV), None, cfg.k, renormalize=True)
+    _, rids, rgate = O.route(x, w.wr, None, cfg.k, renormalize=True)
+    assert torch.equal(ids.cpu(), rids)
+    assert ((gate.cpu().double() - rgate).abs() / rgate).max().item() <= GATE_RTOL
+
+
+# ------------------------------------------------------------------ permute
+
+
+@pytest.mark.parametrize("T,k,E,skew", [(16, 2, 8, False), (1, 4, 60, False), (1000, 6, 64, False),
+                                        (777, 1, 32, True), (300, 1, 1, False), (70, 8, 256, False)])
+def test_permute_bit_exact(M, T, k, E, skew):
+    gen = torch.Generator().manual_seed(T * 31 + k)
+    if skew:   # most rows on expert 3, several experts empty
+        ids = torch.where(torch.rand((T, k), generator=gen) < 0.8, 3,
+                          torch.randint(0, E // 2, (T, k), generator=gen)).to(torch.int32)
+    else:
+        ids = torch.stack([torch.randperm(E, generator=gen)[:k] for _ in range(T)]).to(torch.int32)
+    x = torch.randn((T, 264), generator=gen).to(torch.bfloat16)
+    offsets, perm, inv, xp = M.permute(ids.to(DEV), x.to(DEV), E)
+    _, roff, rperm, rinv = O.sort_by_expert(ids, E)
+    assert torch.equal(offsets.cpu(), roff)
+    assert torch.equal(perm.cpu(), rperm)
+    assert torch.equal(inv.cpu(), rinv)
+    assert torch.equal(xp.cpu(), O.permute_rows(x, rperm, k))
+
+
+def test_unpermute_of_permute_is_identity(M):
+    """k = 1, gate 1: combine(permute(x)) returns x bit-exactly."""
+    gen = torch.Generator().manual_seed(9)
+    T, E = 513, 7
+    ids = torch.randint(0, E, (T, 1), generator=gen).to(torch.int32)
+    x = torch.randn((T, 128), generator=gen).to(torch.float16)
+    _, _, inv, xp = M.permute(ids.to(DEV), x.to(DEV), E)
+    out = M.unpermute_combine(xp, inv, torch.ones((T, 1), device=DEV), None, torch.float16)
+    assert torch.equal(out.cpu(), x)
+
+
+def test_combine_matches_oracle(M):
+    gen = torch.Generator().manual_seed(10)
+    T, k, d = 37, 3, 96
+    y = torch.randn((T * k, d), generator=gen, dtype=torch.float32)
+    inv = torch.randperm(T * k, generator=gen).to(torch.int32)
+    gate = torch.rand((T, k), generator=gen)
+    sh = torch.randn((T, d), generator=gen).to(torch.bfloat16)
+    out = M.unpermute_combine(y.to(DEV), inv.to(DEV), gate.to(DEV), sh.to(DEV), torch.float32).cpu()
+    ref = sum(gate[:, j:j + 1].double() * y.double()[inv.view(T, k)[:, j].long()] for j in range(k)) + sh.double()
+    assert (out.double() - ref).abs().max().item() <= 1e-5 * ref.abs().max().item()
+
+
+# ------------------------------------------------------------------ grouped GEMM
+
+
+def _rows_offsets(counts):
+    off = torch.zeros(len(counts) + 1, dtype=torch.int32)
+    off[1:] = torch.cumsum(torch.tensor(counts), 0)
+    return off
+
+
+def _oracle_gemm(a, q, s, group, offsets, act):
+    out = []
+    for e in range(q.shape[0]):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        w = O.dequant(q[e:e + 1], s[e:e + 1], group)[0] if s is not None else q[e].double()
+        out.append(O.activation(a[lo:hi].double() @ w, act))
+    return torch.cat(out)
+
+
+@pytest.mark.parametrize("bits,group,dtype", [(4, 0, torch.float16), (4, 128, torch.bfloat16),
+                                              (8, 0, torch.float16), (8, 128, torch.bfloat16),
+                                              (4, 128, torch.float16), (16, 0, torch.bfloat16)])
+@pytest.mark.parametrize("counts", [[0, 1, 17, 40], [300, 0, 1250, 3]])
+@pytest.mark.parametrize("act", ["none", "relu"])
+def test_gemm_exact_integers(M, bits, group, dtype, counts, act):
+    """Integer activations and power-of-two scales: every product and fp32 partial sum
+    is exact, so the GPU result equals the oracle bit for bit."""
+    gen = torch.Generator().manual_seed(sum(counts) + bits)
+    E, K, N = len(counts), 512, 192
+    R = sum(counts)
+    a = torch.randint(-1, 2, (R, K), generator=gen).to(dtype)
+    if bits == 16:
+        q = torch.randint(-8, 9, (E, K, N), generator=gen).to(dtype)
+        s = None
+        packed = M.pack_weights(q.to(DEV), None, 16, 0)
+    else:
+        q = _codes(bits, (E, K, N), gen)
+        G = 1 if group == 0 else K // 128
+        s = (2.0 ** torch.randint(-7, -4, (E, G, N), generator=gen).double()).to(dtype)
+        packed = M.pack_weights(q.to(DEV), s.to(DEV), bits, group)
+    off = _rows_offsets(counts)
+    got = M.grouped_gemm(a.to(DEV), packed, bits, E, K, N, group, off.to(DEV), act, torch.float32).cpu()
+    ref = _oracle_gemm(a, q, s, group, off, act)
+    assert torch.equal(got.double(), ref)
+
+
+@pytest.mark.parametrize("name,which", [("tiny", 1), ("tiny", 2), ("encdec_int8", 1), ("encdec_int4", 2),
+                                        ("qwen", 1), ("qwen", 2), ("phi", 1)])
+@pytest.mark.parametrize("counts", [[3, 0, 1, 2], [40, 7, 0, 129]])
+def test_gemm_config_shapes_vs_oracle(M, name, which, counts):
+    """FC1 (with its activation) or FC2 on each config's real (K, N), 4 experts."""
+    cfg = synth.CONFIGS[name]
+    E = len(counts)
+    K, N, act = (cfg.d, cfg.F1, cfg.act) if which == 1 else (cfg.F, cfg.d, "none")
+    q = synth.codes(cfg, "q1" if which == 1 else "q2", (E, K, N))
+    s = synth.scales(cfg, "s1" if which == 1 else "s2", E, K, N)
+    R = sum(counts)
+    a = synth.normal(cfg, "x", (R, K), 1.0, cfg.torch_dtype, extra=which)
+    off = _rows_offsets(counts)
+    packed = M.pack_weights(q.to(DEV), s.to(DEV), cfg.bits, cfg.group)
+    got = M.grouped_gemm(a.to(DEV), packed, cfg.bits, E, K, N, cfg.group, off.to(DEV), act, cfg.torch_dtype)
+    ref = _oracle_gemm(a, q, s, cfg.group, off, act)
+    assert_close_layer(got, ref, f"{name} fc{which}")
+
+
+def test_shared_expert_vs_oracle(M):
+    cfg = synth.CONFIGS["qwen"]
+    w = synth.layer_weights(cfg)
+    for T in (1, 8, 100):
+        x = synth.activations(cfg, T)
+        gu = M.pack_weights(w.ws_gu.to(DEV)[None], None, 16, 0)
+        dn = M.pack_weights(w.ws_d.to(DEV)[None], None, 16, 0)
+        got = M.shared_expert(x.to(DEV), gu, dn, cfg.Fs, torch.float32)
+        assert_close_layer(got, O.shared_expert(x, w.ws_gu, w.ws_d), f"shared T={T}")
+
+
+# ------------------------------------------------------------------ whole layer
+
+
+def _run_layer(M, cfg, w, x, max_T=None):
+    from weight_only_int4_route_gb300.moe import Layer, PackedLayer
+    layer = Layer(PackedLayer.from_weights(cfg, w, DEV), max_T or max(1, x.shape[0]))
+    out = layer.forward(x.to(DEV))
+    torch.cuda.synchronize()
+    return layer, out
+
+
+def _check_layer(M, cfg, T, subset=None):
+    w, x = layer_inputs(cfg, T)
+    layer, out = _run_layer(M, cfg, w, x)
+    ref = O.moe_layer(x, w, cfg, token_subset=subset)
+    rt = layer.routing(T)
+    assert torch.equal(rt["ids"].cpu(), ref["ids"])
+    assert torch.equal(rt["offsets"].cpu(), ref["offsets"])
+    assert torch.equal(rt["perm"].cpu(), ref["perm"])
+    assert torch.equal(rt["inv_perm"].cpu(), ref["inv_perm"])
+    assert ((rt["gate"].cpu().double() - ref["gate"]).abs() / ref["gate"]).max().item() <= GATE_RTOL
+    got = out.cpu() if subset is None else out.cpu()[subset]
+    return assert_close_layer(got, ref["out"], f"{cfg.name} T={T}")
+
+
+@pytest.mark.parametrize("name,T", [("tiny", 16), ("tiny", 1), ("encdec_int8", 40), ("encdec_int4", 40),
+                                    ("encdec_int4", 77), ("qwen", 1), ("qwen", 8), ("qwen", 32),
+                                    ("dsv2", 32), ("phi", 1), ("phi", 16)])
+def test_layer_matches_oracle(M, name, T):
+    _check_layer(M, synth.CONFIGS[name], T)
+
+
+@pytest.mark.parametrize("name,T", [("encdec_int4", 3840), ("encdec_int8", 1280), ("qwen", 4096),
+                                    ("dsv2", 512), ("phi", 8192)])
+def test_layer_full_size_sampled(M, name, T):
+    """Full workload size in the same launch configuration the benchmark times: routing
+    compared in full, outputs on 256 seeded token samples (the layer is per-token
+    independent, so the oracle computes only those tokens)."""
+    subset = torch.randperm(T, generator=torch.Generator().manual_seed(T))[:256].sort().values
+    _check_layer(M, synth.CONFIGS[name], T, subset)
+
+
+def test_layer_edge_cases(M):
+    # single expert (E = 1, k = 1): a dense FFN
+    _check_layer(M, synth.custom("tiny", E=1, k=1, index=7), 33)
+    # every expert selected (k = E)
+    _check_layer(M, synth.custom("tiny", E=4, k=4, index=8), 21)
+    # skewed routing: a huge logit bias sends every token to one expert, the rest are empty
+    cfg = synth.custom("encdec_int4", index=9)
+    w, x = layer_inputs(cfg, 150)
+    w.bias = torch.zeros(cfg.E)
+    w.bias[5] = 100.0
+    layer, out = _run_layer(M, cfg, w, x)
+    ref = O.moe_layer(x, w, cfg)
+    assert int(ref["counts"][5]) == 150
+    assert torch.equal(layer.routing(150)["offsets"].cpu(), ref["offsets"])
+    assert_close_layer(out.cpu(), ref["out"], "skewed")
+
+
+def test_layer_zero_tokens(M):
+    cfg = synth.CONFIGS["tiny"]
+    w, _ = layer_inputs(cfg, 4)
+    from weight_only_int4_route_gb300.moe import Layer, PackedLayer
+    layer = Layer(PackedLayer.from_weights(cfg, w, DEV), 4)
+    x = torch.empty((0, cfg.d), dtype=cfg.torch_dtype, device=DEV)
+    out = layer.forward(x)
+    assert out.shape == (0, cfg.d)

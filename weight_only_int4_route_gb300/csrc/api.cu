@@ -1,0 +1,356 @@
+// Public entry points that chain kernels (grouped GEMM, shared expert, whole layer), the
+// error reporting and the small host helpers.
+#include <stdarg.h>
+#include <stdio.h>
+
+#include <algorithm>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+
+namespace {
+thread_local char g_err[512] = "no error";
+}
+
+int set_error(int code, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int check_launch(const char *what) {
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return set_error(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  return MOE_OK;
+}
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+namespace {
+
+int check_gemm_args(int bits, const void *a, int a_dtype, const void *packed_w, int64_t E, int64_t K,
+                    int64_t N, int group, const int32_t *offsets, int64_t R, int act, const void *out,
+                    int out_dtype) {
+  MOE_REQUIRE(is16(a_dtype), "a_dtype must be MOE_F16 or MOE_BF16");
+  MOE_REQUIRE(out_dtype == MOE_F16 || out_dtype == MOE_BF16 || out_dtype == MOE_F32, "bad out_dtype");
+  MOE_REQUIRE(act >= MOE_ACT_NONE && act <= MOE_ACT_SWIGLU, "bad act %d", act);
+  MOE_REQUIRE(E >= 1 && E <= 256, "need 1 <= E <= 256 (E=%lld)", (long long)E);
+  MOE_REQUIRE(group == 0 || group == 128, "group must be 0 or 128");
+  MOE_REQUIRE(bits != 16 || group == 0, "16-bit weights take no group");
+  MOE_REQUIRE(R >= 0 && R < (int64_t(1) << 31), "R out of range");
+  MOE_REQUIRE(K >= 128 && K % 128 == 0 && K < (int64_t(1) << 30), "K must be a positive multiple of 128 (K=%lld)", (long long)K);
+  if (act == MOE_ACT_SWIGLU)
+    MOE_SUPPORT(N % 64 == 0 && N >= 64, "SWIGLU needs N %% 64 == 0 (N=%lld)", (long long)N);
+  else
+    MOE_SUPPORT(N % 64 == 0 && N >= 64, "N must be a multiple of 64 (N=%lld)", (long long)N);
+  MOE_REQUIRE(N < (int64_t(1) << 30), "N too large");
+  MOE_REQUIRE(offsets != nullptr || E == 1, "offsets may be NULL only when E == 1");
+  if (R == 0) return MOE_OK;
+  MOE_REQUIRE(a && packed_w && out, "null pointer argument");
+  MOE_REQUIRE(aligned16(a) && aligned16(packed_w) && aligned16(out) && (offsets == nullptr || aligned16(offsets)),
+              "pointers must be 16-byte aligned");
+  return MOE_OK;
+}
+
+size_t gemm_ws_bytes(const GemmPlan &pl, int64_t R, int64_t N) {
+  return pl.partial ? align256(size_t(pl.splits) * size_t(R) * size_t(N) * 4) : 0;
+}
+
+int grouped_gemm(int bits, const void *a, int a_dtype, const void *packed_w, int64_t E, int64_t K,
+                 int64_t N, int group, const int32_t *offsets, int64_t R, int act, void *out,
+                 int out_dtype, void *workspace, size_t workspace_bytes, cudaStream_t st) {
+  MOE_TRY(check_gemm_args(bits, a, a_dtype, packed_w, E, K, N, group, offsets, R, act, out, out_dtype));
+  if (R == 0) return MOE_OK;
+  const GemmPlan pl = plan_gemm(R, E, K, N, act, false);
+  const size_t need = gemm_ws_bytes(pl, R, N);
+  if (need) {
+    MOE_REQUIRE(workspace && aligned16(workspace), "workspace must be non-null and 16-byte aligned");
+    if (workspace_bytes < need)
+      return set_error(MOE_ERR_WORKSPACE, "grouped GEMM workspace %zu < %zu bytes", workspace_bytes, need);
+  }
+  GemmArgs g{};
+  g.a = a;
+  g.w = packed_w;
+  g.scales = bits == 16 ? nullptr
+                        : static_cast<const char *>(packed_w) + moe_packed_scale_offset(E, K, N, bits);
+  g.offsets = offsets;
+  g.out = out;
+  g.partial = static_cast<float *>(workspace);
+  g.R = R;
+  g.E = int(E);
+  g.K = int(K);
+  g.N = int(N);
+  g.group = group;
+  g.act = act;
+  g.out_dtype = out_dtype;
+  g.a_dtype = a_dtype;
+  g.bits = bits;
+  MOE_TRY(launch_gemm_mma(g, pl, st));
+  if (pl.partial) MOE_TRY(launch_reduce_act(g.partial, pl.splits, R, int(N), act, out, out_dtype, st));
+  return MOE_OK;
+}
+
+// ---- layer workspace layout -------------------------------------------------------------
+struct LayerPlan {
+  int64_t T, R;
+  GemmPlan fc1, fc2, sh1, sh2;
+  size_t o_ids, o_gate, o_off, o_perm, o_inv, o_pws, o_xp, o_p1, o_h, o_y, o_hs, o_ps1, o_ys, total;
+};
+
+int check_desc(const moe_layer_desc *d) {
+  MOE_REQUIRE(d != nullptr, "desc is NULL");
+  MOE_REQUIRE(is16(d->dtype), "desc.dtype must be MOE_F16 or MOE_BF16");
+  MOE_REQUIRE(d->router_dtype == MOE_F32 || d->router_dtype == d->dtype, "desc.router_dtype must be F32 or dtype");
+  MOE_REQUIRE(d->bits == 4 || d->bits == 8, "desc.bits must be 4 or 8");
+  MOE_REQUIRE(d->group == 0 || d->group == 128, "desc.group must be 0 or 128");
+  MOE_REQUIRE(d->act >= MOE_ACT_RELU && d->act <= MOE_ACT_SWIGLU, "desc.act must be RELU, GELU or SWIGLU");
+  MOE_REQUIRE(d->E >= 1 && d->E <= 256 && d->k >= 1 && d->k <= d->E, "need 1 <= k <= E <= 256");
+  MOE_REQUIRE(d->d >= 128 && d->d % 128 == 0, "d must be a multiple of 128 (d=%lld)", (long long)d->d);
+  MOE_REQUIRE(d->F >= 128 && d->F % 128 == 0, "F must be a multiple of 128 (F=%lld)", (long long)d->F);
+  MOE_REQUIRE(d->Fs >= 0 && (d->Fs == 0 || d->Fs % 128 == 0), "Fs must be 0 or a multiple of 128");
+  return MOE_OK;
+}
+
+LayerPlan plan_layer(const moe_layer_desc *d, int64_t T) {
+  LayerPlan p{};
+  p.T = T;
+  p.R = T * d->k;
+  const int64_t F1 = d->act == MOE_ACT_SWIGLU ? 2 * d->F : d->F;
+  p.fc1 = plan_gemm(p.R, d->E, d->d, F1, d->act, false);
+  p.fc2 = plan_gemm(p.R, d->E, d->F, d->d, MOE_ACT_NONE, true);
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += align256(bytes);
+    return at;
+  };
+  p.o_ids = take(size_t(p.R) * 4);
+  p.o_gate = take(size_t(p.R) * 4);
+  p.o_off = take(size_t(d->E + 1) * 4);
+  p.o_perm = take(size_t(p.R) * 4);
+  p.o_inv = take(size_t(p.R) * 4);
+  p.o_pws = take(moe_permute_workspace_size(T, d->E, d->k));
+  p.o_xp = take(size_t(p.R) * d->d * 2);
+  p.o_p1 = take(p.fc1.partial ? size_t(p.fc1.splits) * p.R * F1 * 4 : 0);
+  p.o_h = take(size_t(p.R) * d->F * 2);
+  p.o_y = take(size_t(p.fc2.splits) * p.R * d->d * 4);
+  if (d->Fs > 0) {
+    p.sh1 = plan_gemm(T, 1, d->d, 2 * d->Fs, MOE_ACT_SWIGLU, false);
+    p.sh2 = plan_gemm(T, 1, d->Fs, d->d, MOE_ACT_NONE, true);
+    p.o_hs = take(size_t(T) * d->Fs * 2);
+    p.o_ps1 = take(p.sh1.partial ? size_t(p.sh1.splits) * T * 2 * d->Fs * 4 : 0);
+    p.o_ys = take(size_t(p.sh2.splits) * T * d->d * 4);
+  }
+  p.total = o;
+  return p;
+}
+
+GemmArgs make_args(int bits, const void *a, int dt, const void *w, int64_t E, int64_t K, int64_t N,
+                   int group, const int32_t *offsets, int64_t R, int act, void *out, int out_dtype,
+                   float *partial) {
+  GemmArgs g{};
+  g.a = a;
+  g.w = w;
+  g.scales = bits == 16 ? nullptr : static_cast<const char *>(w) + moe_packed_scale_offset(E, K, N, bits);
+  g.offsets = offsets;
+  g.out = out;
+  g.partial = partial;
+  g.R = R;
+  g.E = int(E);
+  g.K = int(K);
+  g.N = int(N);
+  g.group = group;
+  g.act = act;
+  g.out_dtype = out_dtype;
+  g.a_dtype = dt;
+  g.bits = bits;
+  return g;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" const char *moe_last_error_string(void) { return g_err; }
+extern "C" int moe_version(void) { return 1; }
+
+extern "C" size_t moe_grouped_gemm_workspace_size(int64_t R, int64_t E, int64_t K, int64_t N, int bits,
+                                                  int act) {
+  (void)bits;
+  if (R <= 0 || E < 1 || K < 128 || N < 64) return 0;
+  return gemm_ws_bytes(plan_gemm(R, E, K, N, act, false), R, N);
+}
+
+extern "C" int moe_grouped_gemm_w4a16(const void *a, int a_dtype, const void *packed_w, int64_t E,
+                                      int64_t K, int64_t N, int group, const int32_t *offsets, int64_t R,
+                                      int act, void *out, int out_dtype, void *workspace,
+                                      size_t workspace_bytes, moe_stream_t stream) {
+  return grouped_gemm(4, a, a_dtype, packed_w, E, K, N, group, offsets, R, act, out, out_dtype, workspace,
+                      workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int moe_grouped_gemm_w8a16(const void *a, int a_dtype, const void *packed_w, int64_t E,
+                                      int64_t K, int64_t N, int group, const int32_t *offsets, int64_t R,
+                                      int act, void *out, int out_dtype, void *workspace,
+                                      size_t workspace_bytes, moe_stream_t stream) {
+  return grouped_gemm(8, a, a_dtype, packed_w, E, K, N, group, offsets, R, act, out, out_dtype, workspace,
+                      workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int moe_grouped_gemm_w16a16(const void *a, int a_dtype, const void *packed_w, int64_t E,
+                                       int64_t K, int64_t N, const int32_t *offsets, int64_t R, int act,
+                                       void *out, int out_dtype, void *workspace, size_t workspace_bytes,
+                                       moe_stream_t stream) {
+  return grouped_gemm(16, a, a_dtype, packed_w, E, K, N, 0, offsets, R, act, out, out_dtype, workspace,
+                      workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" size_t moe_shared_expert_workspace_size(int64_t T, int64_t d, int64_t Fs) {
+  if (T <= 0 || d < 128 || Fs < 128) return 0;
+  const GemmPlan p1 = plan_gemm(T, 1, d, 2 * Fs, MOE_ACT_SWIGLU, false);
+  const GemmPlan p2 = plan_gemm(T, 1, Fs, d, MOE_ACT_NONE, true);
+  return align256(size_t(T) * Fs * 2) + gemm_ws_bytes(p1, T, 2 * Fs) + gemm_ws_bytes(p2, T, d);
+}
+
+extern "C" int moe_shared_expert(const void *x, int x_dtype, const void *w_gate_up_packed,
+                                 const void *w_down_packed, int64_t T, int64_t d, int64_t Fs, void *out,
+                                 int out_dtype, void *workspace, size_t workspace_bytes,
+                                 moe_stream_t stream) {
+  MOE_REQUIRE(out_dtype == MOE_F32 || out_dtype == x_dtype, "out_dtype must be F32 or the x dtype");
+  MOE_TRY(check_gemm_args(16, x, x_dtype, w_gate_up_packed, 1, d, 2 * Fs, 0, nullptr, T, MOE_ACT_SWIGLU, out, out_dtype));
+  MOE_TRY(check_gemm_args(16, x, x_dtype, w_down_packed, 1, Fs, d, 0, nullptr, T, MOE_ACT_NONE, out, out_dtype));
+  if (T == 0) return MOE_OK;
+  const size_t need = moe_shared_expert_workspace_size(T, d, Fs);
+  MOE_REQUIRE(workspace && aligned16(workspace), "workspace must be non-null and 16-byte aligned");
+  if (workspace_bytes < need)
+    return set_error(MOE_ERR_WORKSPACE, "shared-expert workspace %zu < %zu bytes", workspace_bytes, need);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const GemmPlan p1 = plan_gemm(T, 1, d, 2 * Fs, MOE_ACT_SWIGLU, false);
+  const GemmPlan p2 = plan_gemm(T, 1, Fs, d, MOE_ACT_NONE, true);
+  char *ws = static_cast<char *>(workspace);
+  void *hs = ws;
+  float *pa = reinterpret_cast<float *>(ws + align256(size_t(T) * Fs * 2));
+  float *pb = reinterpret_cast<float *>(reinterpret_cast<char *>(pa) + gemm_ws_bytes(p1, T, 2 * Fs));
+  MOE_TRY(launch_gemm_mma(make_args(16, x, x_dtype, w_gate_up_packed, 1, d, 2 * Fs, 0, nullptr, T,
+                                    MOE_ACT_SWIGLU, hs, x_dtype, pa), p1, st));
+  if (p1.partial) MOE_TRY(launch_reduce_act(pa, p1.splits, T, int(2 * Fs), MOE_ACT_SWIGLU, hs, x_dtype, st));
+  MOE_TRY(launch_gemm_mma(make_args(16, hs, x_dtype, w_down_packed, 1, Fs, d, 0, nullptr, T,
+                                    MOE_ACT_NONE, nullptr, MOE_F32, pb), p2, st));
+  return launch_reduce_act(pb, p2.splits, T, int(d), MOE_ACT_NONE, out, out_dtype, st);
+}
+
+extern "C" size_t moe_layer_workspace_size(const moe_layer_desc *desc, int64_t T) {
+  if (check_desc(desc) != MOE_OK || T < 0) return 0;
+  return plan_layer(desc, T).total;
+}
+
+extern "C" int moe_layer_routing_view(const moe_layer_desc *desc, int64_t T, void *workspace,
+                                      moe_layer_routing *view) {
+  MOE_TRY(check_desc(desc));
+  MOE_REQUIRE(T >= 0 && workspace && view, "bad arguments");
+  const LayerPlan p = plan_layer(desc, T);
+  char *ws = static_cast<char *>(workspace);
+  view->ids = reinterpret_cast<int32_t *>(ws + p.o_ids);
+  view->gate_w = reinterpret_cast<float *>(ws + p.o_gate);
+  view->offsets = reinterpret_cast<int32_t *>(ws + p.o_off);
+  view->perm = reinterpret_cast<int32_t *>(ws + p.o_perm);
+  view->inv_perm = reinterpret_cast<int32_t *>(ws + p.o_inv);
+  return MOE_OK;
+}
+
+extern "C" int moe_layer_launch_count(const moe_layer_desc *desc, int64_t T) {
+  if (check_desc(desc) != MOE_OK || T <= 0) return 0;
+  const LayerPlan p = plan_layer(desc, T);
+  int n = 1 /*route*/ + 3 /*count, scan, scatter*/ + 1 /*fc1*/ + (p.fc1.partial ? 1 : 0) + 1 /*fc2*/ + 1 /*combine*/;
+  if (desc->Fs > 0) n += 2 + (p.sh1.partial ? 1 : 0);
+  return n;
+}
+
+extern "C" int moe_layer_forward(const moe_layer_desc *desc, const moe_layer_weights *w, const void *x,
+                                 int64_t T, void *out, void *workspace, size_t workspace_bytes,
+                                 moe_stream_t stream) {
+  return moe_layer_forward_profiled(desc, w, x, T, out, workspace, workspace_bytes, stream, nullptr);
+}
+
+extern "C" int moe_layer_forward_profiled(const moe_layer_desc *desc, const moe_layer_weights *w,
+                                          const void *x, int64_t T, void *out, void *workspace,
+                                          size_t workspace_bytes, moe_stream_t stream,
+                                          void *const *stage_events) {
+  MOE_TRY(check_desc(desc));
+  MOE_REQUIRE(w != nullptr, "weights struct is NULL");
+  MOE_REQUIRE(T >= 0 && T * desc->k < (int64_t(1) << 31), "T out of range");
+  if (T == 0) return MOE_OK;
+  MOE_REQUIRE(x && out && w->w_router && w->w1 && w->w2, "null pointer argument");
+  MOE_REQUIRE(desc->Fs == 0 || (w->ws_gate_up && w->ws_down), "shared-expert weights missing");
+  const LayerPlan p = plan_layer(desc, T);
+  MOE_REQUIRE(workspace && aligned16(workspace), "workspace must be non-null and 16-byte aligned");
+  if (workspace_bytes < p.total)
+    return set_error(MOE_ERR_WORKSPACE, "layer workspace %zu < %zu bytes", workspace_bytes, p.total);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char *ws = static_cast<char *>(workspace);
+  int32_t *ids = reinterpret_cast<int32_t *>(ws + p.o_ids);
+  float *gate = reinterpret_cast<float *>(ws + p.o_gate);
+  int32_t *offs = reinterpret_cast<int32_t *>(ws + p.o_off);
+  int32_t *perm = reinterpret_cast<int32_t *>(ws + p.o_perm);
+  int32_t *inv = reinterpret_cast<int32_t *>(ws + p.o_inv);
+  void *xp = ws + p.o_xp;
+  float *p1 = reinterpret_cast<float *>(ws + p.o_p1);
+  void *h = ws + p.o_h;
+  float *y = reinterpret_cast<float *>(ws + p.o_y);
+  const int dt = desc->dtype;
+  const int64_t d = desc->d, F = desc->F, E = desc->E;
+  const int k = desc->k;
+  const int64_t F1 = desc->act == MOE_ACT_SWIGLU ? 2 * F : F;
+
+  auto mark = [&](int stage) -> int {
+    if (!stage_events) return MOE_OK;
+    if (cudaEventRecord(static_cast<cudaEvent_t>(stage_events[stage]), st) != cudaSuccess)
+      return check_launch("stage event");
+    return MOE_OK;
+  };
+  MOE_TRY(mark(MOE_STAGE_START));
+  MOE_TRY(moe_route_topk(x, dt, w->w_router, desc->router_dtype, w->router_bias, T, d, E, k,
+                         desc->renormalize, ids, gate, stream));
+  MOE_TRY(mark(MOE_STAGE_ROUTED));
+  MOE_TRY(moe_permute(ids, x, dt, T, d, E, k, offs, perm, inv, xp, ws + p.o_pws,
+                      moe_permute_workspace_size(T, E, k), stream));
+  MOE_TRY(mark(MOE_STAGE_PERMUTED));
+  MOE_TRY(launch_gemm_mma(make_args(desc->bits, xp, dt, w->w1, E, d, F1, desc->group, offs, p.R, desc->act,
+                                    h, dt, p1), p.fc1, st));
+  if (p.fc1.partial) MOE_TRY(launch_reduce_act(p1, p.fc1.splits, p.R, int(F1), desc->act, h, dt, st));
+  MOE_TRY(mark(MOE_STAGE_FC1));
+  MOE_TRY(launch_gemm_mma(make_args(desc->bits, h, dt, w->w2, E, F, d, desc->group, offs, p.R, MOE_ACT_NONE,
+                                    nullptr, MOE_F32, y), p.fc2, st));
+  MOE_TRY(mark(MOE_STAGE_FC2));
+  const void *sh = nullptr;
+  int shs = 0;
+  if (desc->Fs > 0) {
+    void *hs = ws + p.o_hs;
+    float *ps1 = reinterpret_cast<float *>(ws + p.o_ps1);
+    float *ys = reinterpret_cast<float *>(ws + p.o_ys);
+    MOE_TRY(launch_gemm_mma(make_args(16, x, dt, w->ws_gate_up, 1, d, 2 * desc->Fs, 0, nullptr, T,
+                                      MOE_ACT_SWIGLU, hs, dt, ps1), p.sh1, st));
+    if (p.sh1.partial) MOE_TRY(launch_reduce_act(ps1, p.sh1.splits, T, int(2 * desc->Fs), MOE_ACT_SWIGLU, hs, dt, st));
+    MOE_TRY(launch_gemm_mma(make_args(16, hs, dt, w->ws_down, 1, desc->Fs, d, 0, nullptr, T, MOE_ACT_NONE,
+                                      nullptr, MOE_F32, ys), p.sh2, st));
+    sh = ys;
+    shs = p.sh2.splits;
+  }
+  MOE_TRY(mark(MOE_STAGE_SHARED));
+  MOE_TRY(launch_combine(y, MOE_F32, p.fc2.splits, inv, gate, sh, MOE_F32, shs, T, d, k, out, dt, st));
+  return mark(MOE_STAGE_DONE);
+}

@@ -1,0 +1,234 @@
+// Internal helpers shared by the libmoe translation units (device and host).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------- host side
+
+int set_error(int code, const char *fmt, ...);
+int check_launch(const char *what);  // MOE_OK or MOE_ERR_CUDA with the runtime's message
+int num_sms();                       // SM count of the current device (cached)
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+inline bool is16(int dt) { return dt == MOE_F16 || dt == MOE_BF16; }
+inline size_t dtype_size(int dt) { return dt == MOE_F32 ? 4 : 2; }
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+#define MOE_REQUIRE(cond, ...)                                        \
+  do {                                                                \
+    if (!(cond)) return ::moe::set_error(MOE_ERR_INVALID_ARG, __VA_ARGS__); \
+  } while (0)
+#define MOE_SUPPORT(cond, ...)                                        \
+  do {                                                                \
+    if (!(cond)) return ::moe::set_error(MOE_ERR_UNSUPPORTED, __VA_ARGS__); \
+  } while (0)
+#define MOE_TRY(expr)            \
+  do {                           \
+    int _st = (expr);            \
+    if (_st != MOE_OK) return _st; \
+  } while (0)
+
+// Packed-weight geometry (see include/moe.h).
+inline size_t packed_code_bytes(int64_t E, int64_t K, int64_t N, int bits) {
+  return size_t(E) * size_t(N) * size_t(K) * size_t(bits) / 8;
+}
+inline int64_t scale_groups(int64_t K, int group) { return group == 0 ? 1 : K / group; }
+
+// Split-K / tiling plan of the mma.sync grouped GEMM (shared by size queries and launches).
+struct GemmPlan {
+  int mb;      // m16 tiles per CTA tile (rows per tile = 16 * mb)
+  int splits;  // split-K factor
+  int ks;      // K per split (multiple of 128)
+  int ncb;     // channel blocks
+  bool partial;  // fp32 partial slices instead of the fused epilogue
+};
+GemmPlan plan_gemm(int64_t R, int64_t E, int64_t K, int64_t N, int act, bool want_partial);
+
+struct GemmArgs {
+  const void *a;
+  const void *w;       // code / 16-bit weight region of the packed buffer
+  const void *scales;  // scale region or nullptr
+  const int32_t *offsets;
+  void *out;
+  float *partial;
+  int64_t R;
+  int E, K, N;
+  int group;
+  int act;
+  int out_dtype;
+  int a_dtype;
+  int bits;
+};
+// Enqueue the grouped GEMM described by `g` with plan `pl`.  When pl.partial, the fp32
+// accumulators (times per-channel scales) go to g.partial (splits, R, N).
+int launch_gemm_mma(const GemmArgs &g, const GemmPlan &pl, cudaStream_t st);
+// out[r, c] = act(sum_s part[s, r, c]) (SWIGLU pairs column c with c + N/2).
+int launch_reduce_act(const float *part, int splits, int64_t R, int N, int act, void *out,
+                      int out_dtype, cudaStream_t st);
+// Combine with split slices: out[t] = sum_j g[t,j] * sum_s y[s, inv[t*k+j]] + sum_s sh[s, t].
+int launch_combine(const void *y, int y_dtype, int ysplits, const int32_t *inv_perm,
+                   const float *gate, const void *sh, int sh_dtype, int shsplits, int64_t T,
+                   int64_t d, int k, void *out, int out_dtype, cudaStream_t st);
+
+// ---------------------------------------------------------------- device side
+
+template <typename T> struct Vec2;
+template <> struct Vec2<__half> { using type = __half2; };
+template <> struct Vec2<__nv_bfloat16> { using type = __nv_bfloat162; };
+
+__device__ __forceinline__ float to_f32(__half v) { return __half2float(v); }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+__device__ __forceinline__ float to_f32(float v) { return v; }
+
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ __half from_f32<__half>(float v) { return __float2half_rn(v); }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+  return __float2bfloat16_rn(v);
+}
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+
+__device__ __forceinline__ uint32_t h2_as_u32(__half2 v) { return *reinterpret_cast<uint32_t *>(&v); }
+__device__ __forceinline__ uint32_t h2_as_u32(__nv_bfloat162 v) {
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+__device__ __forceinline__ __half2 u32_as_h2(uint32_t v) { return *reinterpret_cast<__half2 *>(&v); }
+__device__ __forceinline__ __nv_bfloat162 u32_as_b2(uint32_t v) {
+  return *reinterpret_cast<__nv_bfloat162 *>(&v);
+}
+
+// ---- magic-number integer-to-float ("optimized I2F", FT-MoE review section 3) ----------
+// An fp16 with exponent field 1024 keeps an integer 0 <= u < 1024 exactly in its mantissa:
+// OR-ing u into 0x6400 gives 1024 + u.  bf16 keeps only 7 mantissa bits, so 128.0 (0x4300)
+// is the magic there and u must stay below 128.
+
+// INT4 word -> four 16-bit pairs (e0,e1) (e2,e3) (e4,e5) (e6,e7) holding q = u - 8.
+// Pair p lives in bits 4p and 16 + 4p (nibble slots p and p + 4 of the interleaved word).
+__device__ __forceinline__ void i2f_int4(uint32_t w, uint32_t (&h)[4], __half) {
+  const uint32_t magic = 0x64006400u;
+  const uint32_t w8 = w >> 8;
+  const uint32_t t0 = (w & 0x000F000Fu) | magic;   // 1024 + u
+  const uint32_t t1 = (w & 0x00F000F0u) | magic;   // 1024 + 16 u   (upper nibble kept in place)
+  const uint32_t t2 = (w8 & 0x000F000Fu) | magic;
+  const uint32_t t3 = (w8 & 0x00F000F0u) | magic;
+  const __half2 bias = __half2half2(__ushort_as_half(0x6408));      // 1032 = 1024 + 8
+  const __half2 sixteenth = __half2half2(__ushort_as_half(0x2C00));  // 1/16
+  const __half2 bias16 = __half2half2(__ushort_as_half(0xD480));     // -72 = -(64 + 8)
+  h[0] = h2_as_u32(__hsub2(u32_as_h2(t0), bias));
+  h[1] = h2_as_u32(__hfma2(u32_as_h2(t1), sixteenth, bias16));
+  h[2] = h2_as_u32(__hsub2(u32_as_h2(t2), bias));
+  h[3] = h2_as_u32(__hfma2(u32_as_h2(t3), sixteenth, bias16));
+}
+
+__device__ __forceinline__ void i2f_int4(uint32_t w, uint32_t (&h)[4], __nv_bfloat16) {
+  const uint32_t magic = 0x43004300u;                                    // 128.0 in bf16
+  const __nv_bfloat162 bias = __bfloat162bfloat162(__ushort_as_bfloat16(0x4308));  // 136 = 128 + 8
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    const uint32_t t = ((w >> (4 * p)) & 0x000F000Fu) | magic;           // 128 + u
+    h[p] = h2_as_u32(__hsub2(u32_as_b2(t), bias));
+  }
+}
+
+// INT8 word (byte b = element b, u = q + 128) -> two pairs (e0,e1) (e2,e3).
+__device__ __forceinline__ void i2f_int8(uint32_t w, uint32_t (&h)[2], __half) {
+  const uint32_t t0 = __byte_perm(w, 0x64646464u, 0x5140);  // [u0, 0x64, u1, 0x64] = 1024 + u
+  const uint32_t t1 = __byte_perm(w, 0x64646464u, 0x5342);
+  const __half2 bias = __half2half2(__ushort_as_half(0x6480));  // 1152 = 1024 + 128
+  h[0] = h2_as_u32(__hsub2(u32_as_h2(t0), bias));
+  h[1] = h2_as_u32(__hsub2(u32_as_h2(t1), bias));
+}
+
+// bf16 cannot hold a byte in its mantissa; go through the fp32 magic 2^23 (exact for
+// |q| <= 128, which also fits bf16's 8 significant bits).
+__device__ __forceinline__ float i2f_int8_byte_f32(uint32_t w, int b) {
+  const uint32_t sel = 0x7540u | uint32_t(b);                 // [u_b, 0, 0, 0x4B]
+  return __uint_as_float(__byte_perm(w, 0x4B000000u, sel)) - 8388736.0f;  // 2^23 + 128
+}
+__device__ __forceinline__ void i2f_int8(uint32_t w, uint32_t (&h)[2], __nv_bfloat16) {
+  h[0] = h2_as_u32(__floats2bfloat162_rn(i2f_int8_byte_f32(w, 0), i2f_int8_byte_f32(w, 1)));
+  h[1] = h2_as_u32(__floats2bfloat162_rn(i2f_int8_byte_f32(w, 2), i2f_int8_byte_f32(w, 3)));
+}
+
+// Multiply a pair by a broadcast scale: RN(q * s), one rounding of the exact product.
+__device__ __forceinline__ uint32_t scale_pair(uint32_t h, uint32_t s2, __half) {
+  return h2_as_u32(__hmul2(u32_as_h2(h), u32_as_h2(s2)));
+}
+__device__ __forceinline__ uint32_t scale_pair(uint32_t h, uint32_t s2, __nv_bfloat16) {
+  return h2_as_u32(__hmul2(u32_as_b2(h), u32_as_b2(s2)));
+}
+
+// ---- activations ----------------------------------------------------------------------
+__device__ __forceinline__ float act_relu(float x) { return fmaxf(x, 0.0f); }
+__device__ __forceinline__ float act_gelu(float x) {  // exact erf form
+  return 0.5f * x * (1.0f + erff(x * 0.70710678118654752440f));
+}
+__device__ __forceinline__ float act_silu(float x) { return x / (1.0f + expf(-x)); }
+__device__ __forceinline__ float act_apply(float x, int act) {
+  return act == MOE_ACT_RELU ? act_relu(x) : (act == MOE_ACT_GELU ? act_gelu(x) : x);
+}
+
+// ---- warp-level tensor-core MMA (m16n8k16, fp32 accumulate) ---------------------------
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1, __half) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1, __nv_bfloat16) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// ---- cp.async (8-byte, zero-fill when src_bytes == 0) ----------------------------------
+__device__ __forceinline__ void cp_async8(void *smem, const void *gmem, int src_bytes) {
+  const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;\n" ::"r"(s), "l"(gmem), "r"(src_bytes));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N> __device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+// Exclusive prefix sum over blockDim.x (<= 1024, multiple of 32) ints; returns the total.
+__device__ __forceinline__ int block_exclusive_scan(int v, int *out, int *scratch /*32 ints*/) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) scratch[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int s = lane < nw ? scratch[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    scratch[lane] = s;  // inclusive over warps
+  }
+  __syncthreads();
+  const int base = warp > 0 ? scratch[warp - 1] : 0;
+  *out = base + x - v;
+  const int total = scratch[nw - 1];
+  __syncthreads();
+  return total;
+}
+
+}  // namespace moe
