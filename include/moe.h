@@ -62,6 +62,13 @@ const char *moe_last_error_string(void);
 /* ABI version (bumped on any incompatible change). */
 int moe_version(void);
 
+/* Device-side status.  Kernels that wait on on-chip barriers bound every wait (about a
+ * second); when one expires the kernel records a nonzero code in a device word, drains its
+ * own asynchronous work, releases its tensor memory and returns early (its outputs are then
+ * incomplete).  This call synchronizes `stream`, copies the code to *host_code (0 = no
+ * error) and clears it. */
+int moe_device_error(moe_stream_t stream, int32_t *host_code);
+
 /* ------------------------------------------------------------------------------------
  * Weight packing.  [FT] Algorithm 1: W (E, M, N) integer codes, M = reduction dim,
  * N = output channel; scales S (E, 1, N) per output channel.  [Specter] GPTQ: group size
@@ -152,6 +159,9 @@ int moe_permute(const int32_t *ids, const void *x, int x_dtype, int64_t T, int64
  * Per-channel scales are applied to the fp32 accumulator (an exact reformulation of
  * Algorithm 1 up to rounding order); group-128 scales are applied in the mainloop as
  * RN(q * s) in the operand dtype, as Algorithm 1 states. */
+/* Which kernel a grouped GEMM with these arguments (offsets given) runs: 1 = the tcgen05
+ * tensor-memory kernel (many rows per expert), 0 = the warp-MMA kernel (decode batches). */
+int moe_gemm_path(int64_t R, int64_t E, int64_t K, int64_t N, int bits, int group, int act);
 size_t moe_grouped_gemm_workspace_size(int64_t R, int64_t E, int64_t K, int64_t N, int bits,
                                        int act);
 int moe_grouped_gemm_w4a16(const void *a, int a_dtype, const void *packed_w, int64_t E, int64_t K,

@@ -194,13 +194,14 @@ def _oracle_gemm(a, q, s, group, offsets, act):
 @pytest.mark.parametrize("bits,group,dtype", [(4, 0, torch.float16), (4, 128, torch.bfloat16),
                                               (8, 0, torch.float16), (8, 128, torch.bfloat16),
                                               (4, 128, torch.float16), (16, 0, torch.bfloat16)])
-@pytest.mark.parametrize("counts", [[0, 1, 17, 40], [300, 0, 1250, 3]])
+@pytest.mark.parametrize("counts,N", [([0, 1, 17, 40], 192), ([300, 0, 1250, 3], 192), ([300, 0, 1250, 3], 256),
+                                      ([130, 129, 128, 64, 1], 384)])
 @pytest.mark.parametrize("act", ["none", "relu"])
-def test_gemm_exact_integers(M, bits, group, dtype, counts, act):
+def test_gemm_exact_integers(M, bits, group, dtype, counts, N, act):
     """Integer activations and power-of-two scales: every product and fp32 partial sum
-    is exact, so the GPU result equals the oracle bit for bit."""
+    is exact, so the GPU result equals the oracle bit for bit (both kernels)."""
     gen = torch.Generator().manual_seed(sum(counts) + bits)
-    E, K, N = len(counts), 512, 192
+    E, K = len(counts), 512
     R = sum(counts)
     a = torch.randint(-1, 2, (R, K), generator=gen).to(dtype)
     if bits == 16:
@@ -213,14 +214,18 @@ def test_gemm_exact_integers(M, bits, group, dtype, counts, act):
         s = (2.0 ** torch.randint(-7, -4, (E, G, N), generator=gen).double()).to(dtype)
         packed = M.pack_weights(q.to(DEV), s.to(DEV), bits, group)
     off = _rows_offsets(counts)
+    path = M.gemm_path(R, E, K, N, bits, group, act)
+    if bits != 16 and N % 128 == 0 and R / max(1, sum(c > 0 for c in counts)) >= 64:
+        assert path == "tcgen05"
     got = M.grouped_gemm(a.to(DEV), packed, bits, E, K, N, group, off.to(DEV), act, torch.float32).cpu()
+    assert M.device_error(DEV) == 0
     ref = _oracle_gemm(a, q, s, group, off, act)
-    assert torch.equal(got.double(), ref)
+    assert torch.equal(got.double(), ref), path
 
 
 @pytest.mark.parametrize("name,which", [("tiny", 1), ("tiny", 2), ("encdec_int8", 1), ("encdec_int4", 2),
                                         ("qwen", 1), ("qwen", 2), ("phi", 1)])
-@pytest.mark.parametrize("counts", [[3, 0, 1, 2], [40, 7, 0, 129]])
+@pytest.mark.parametrize("counts", [[3, 0, 1, 2], [40, 7, 0, 129], [300, 150, 0, 77]])
 def test_gemm_config_shapes_vs_oracle(M, name, which, counts):
     """FC1 (with its activation) or FC2 on each config's real (K, N), 4 experts."""
     cfg = synth.CONFIGS[name]
@@ -234,7 +239,8 @@ def test_gemm_config_shapes_vs_oracle(M, name, which, counts):
     packed = M.pack_weights(q.to(DEV), s.to(DEV), cfg.bits, cfg.group)
     got = M.grouped_gemm(a.to(DEV), packed, cfg.bits, E, K, N, cfg.group, off.to(DEV), act, cfg.torch_dtype)
     ref = _oracle_gemm(a, q, s, cfg.group, off, act)
-    assert_close_layer(got, ref, f"{name} fc{which}")
+    assert M.device_error(DEV) == 0
+    assert_close_layer(got, ref, f"{name} fc{which} {M.gemm_path(R, E, K, N, cfg.bits, cfg.group, act)}")
 
 
 def test_shared_expert_vs_oracle(M):
@@ -269,6 +275,7 @@ def _check_layer(M, cfg, T, subset=None):
     assert torch.equal(rt["perm"].cpu(), ref["perm"])
     assert torch.equal(rt["inv_perm"].cpu(), ref["inv_perm"])
     assert ((rt["gate"].cpu().double() - ref["gate"]).abs() / ref["gate"]).max().item() <= GATE_RTOL
+    assert M.device_error(DEV) == 0
     got = out.cpu() if subset is None else out.cpu()[subset]
     return assert_close_layer(got, ref["out"], f"{cfg.name} T={T}")
 

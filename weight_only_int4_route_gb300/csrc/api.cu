@@ -98,7 +98,7 @@ int grouped_gemm(int bits, const void *a, int a_dtype, const void *packed_w, int
   g.out_dtype = out_dtype;
   g.a_dtype = a_dtype;
   g.bits = bits;
-  MOE_TRY(launch_gemm_mma(g, pl, st));
+  MOE_TRY(launch_gemm(g, pl, st));
   if (pl.partial) MOE_TRY(launch_reduce_act(g.partial, pl.splits, R, int(N), act, out, out_dtype, st));
   return MOE_OK;
 }
@@ -186,7 +186,24 @@ GemmArgs make_args(int bits, const void *a, int dt, const void *w, int64_t E, in
 using namespace moe;
 
 extern "C" const char *moe_last_error_string(void) { return g_err; }
+
+extern "C" int moe_device_error(moe_stream_t stream, int32_t *host_code) {
+  MOE_REQUIRE(host_code != nullptr, "host_code is NULL");
+  int v = 0;
+  MOE_TRY(read_device_error(reinterpret_cast<cudaStream_t>(stream), &v));
+  *host_code = v;
+  return MOE_OK;
+}
 extern "C" int moe_version(void) { return 1; }
+
+extern "C" int moe_gemm_path(int64_t R, int64_t E, int64_t K, int64_t N, int bits, int group, int act) {
+  if (R <= 0 || E < 1 || K < 128 || N < 64) return 0;
+  const GemmPlan pl = plan_gemm(R, E, K, N, act, false);
+  static const int32_t dummy = 0;
+  const GemmArgs g = make_args(bits, nullptr, MOE_F16, nullptr, E, K, N, group, &dummy, R, act, nullptr,
+                               MOE_F16, nullptr);
+  return (pl.tc && tc_supported(g)) ? 1 : 0;
+}
 
 extern "C" size_t moe_grouped_gemm_workspace_size(int64_t R, int64_t E, int64_t K, int64_t N, int bits,
                                                   int act) {
@@ -245,10 +262,10 @@ extern "C" int moe_shared_expert(const void *x, int x_dtype, const void *w_gate_
   void *hs = ws;
   float *pa = reinterpret_cast<float *>(ws + align256(size_t(T) * Fs * 2));
   float *pb = reinterpret_cast<float *>(reinterpret_cast<char *>(pa) + gemm_ws_bytes(p1, T, 2 * Fs));
-  MOE_TRY(launch_gemm_mma(make_args(16, x, x_dtype, w_gate_up_packed, 1, d, 2 * Fs, 0, nullptr, T,
+  MOE_TRY(launch_gemm(make_args(16, x, x_dtype, w_gate_up_packed, 1, d, 2 * Fs, 0, nullptr, T,
                                     MOE_ACT_SWIGLU, hs, x_dtype, pa), p1, st));
   if (p1.partial) MOE_TRY(launch_reduce_act(pa, p1.splits, T, int(2 * Fs), MOE_ACT_SWIGLU, hs, x_dtype, st));
-  MOE_TRY(launch_gemm_mma(make_args(16, hs, x_dtype, w_down_packed, 1, Fs, d, 0, nullptr, T,
+  MOE_TRY(launch_gemm(make_args(16, hs, x_dtype, w_down_packed, 1, Fs, d, 0, nullptr, T,
                                     MOE_ACT_NONE, nullptr, MOE_F32, pb), p2, st));
   return launch_reduce_act(pb, p2.splits, T, int(d), MOE_ACT_NONE, out, out_dtype, st);
 }
@@ -329,11 +346,11 @@ extern "C" int moe_layer_forward_profiled(const moe_layer_desc *desc, const moe_
   MOE_TRY(moe_permute(ids, x, dt, T, d, E, k, offs, perm, inv, xp, ws + p.o_pws,
                       moe_permute_workspace_size(T, E, k), stream));
   MOE_TRY(mark(MOE_STAGE_PERMUTED));
-  MOE_TRY(launch_gemm_mma(make_args(desc->bits, xp, dt, w->w1, E, d, F1, desc->group, offs, p.R, desc->act,
+  MOE_TRY(launch_gemm(make_args(desc->bits, xp, dt, w->w1, E, d, F1, desc->group, offs, p.R, desc->act,
                                     h, dt, p1), p.fc1, st));
   if (p.fc1.partial) MOE_TRY(launch_reduce_act(p1, p.fc1.splits, p.R, int(F1), desc->act, h, dt, st));
   MOE_TRY(mark(MOE_STAGE_FC1));
-  MOE_TRY(launch_gemm_mma(make_args(desc->bits, h, dt, w->w2, E, F, d, desc->group, offs, p.R, MOE_ACT_NONE,
+  MOE_TRY(launch_gemm(make_args(desc->bits, h, dt, w->w2, E, F, d, desc->group, offs, p.R, MOE_ACT_NONE,
                                     nullptr, MOE_F32, y), p.fc2, st));
   MOE_TRY(mark(MOE_STAGE_FC2));
   const void *sh = nullptr;
@@ -342,10 +359,10 @@ extern "C" int moe_layer_forward_profiled(const moe_layer_desc *desc, const moe_
     void *hs = ws + p.o_hs;
     float *ps1 = reinterpret_cast<float *>(ws + p.o_ps1);
     float *ys = reinterpret_cast<float *>(ws + p.o_ys);
-    MOE_TRY(launch_gemm_mma(make_args(16, x, dt, w->ws_gate_up, 1, d, 2 * desc->Fs, 0, nullptr, T,
+    MOE_TRY(launch_gemm(make_args(16, x, dt, w->ws_gate_up, 1, d, 2 * desc->Fs, 0, nullptr, T,
                                       MOE_ACT_SWIGLU, hs, dt, ps1), p.sh1, st));
     if (p.sh1.partial) MOE_TRY(launch_reduce_act(ps1, p.sh1.splits, T, int(2 * desc->Fs), MOE_ACT_SWIGLU, hs, dt, st));
-    MOE_TRY(launch_gemm_mma(make_args(16, hs, dt, w->ws_down, 1, desc->Fs, d, 0, nullptr, T, MOE_ACT_NONE,
+    MOE_TRY(launch_gemm(make_args(16, hs, dt, w->ws_down, 1, desc->Fs, d, 0, nullptr, T, MOE_ACT_NONE,
                                       nullptr, MOE_F32, ys), p.sh2, st));
     sh = ys;
     shs = p.sh2.splits;

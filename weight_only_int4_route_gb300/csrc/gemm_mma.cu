@@ -38,6 +38,7 @@ constexpr int kKC = 128;        // reduction chunk
 constexpr int kRowBytes = kKC * 2 + 32;
 constexpr int kMaxE = 256;
 constexpr int kEpStride = kNB + 8;  // fp32 epilogue tile row stride
+constexpr int kTcMinRows = 64;      // rows per active expert from which the tcgen05 path is used
 
 template <int BITS> struct WT {
   static constexpr int kVec = BITS == 4 ? 1 : (BITS == 8 ? 2 : 4);  // uint4 per lane per chunk
@@ -336,13 +337,27 @@ GemmPlan plan_gemm(int64_t R, int64_t E, int64_t K, int64_t N, int act, bool wan
   const int64_t tiles = est_tiles(R, E, 16 * pl.mb);
   int64_t S = 1;
   const int64_t target = 2 * int64_t(num_sms());
-  while (S * 2 <= std::max<int64_t>(1, nck / 2) && tiles * ncb_fused * S < target) S *= 2;
+  const bool tc_rows = avg >= kTcMinRows;  // the tcgen05 kernel takes these whole, without split-K
+  while (!tc_rows && S * 2 <= std::max<int64_t>(1, nck / 2) && tiles * ncb_fused * S < target) S *= 2;
   const int64_t cps = cdiv(nck, S);
   pl.ks = int(cps * kKC);
   pl.splits = int(cdiv(nck, cps));
   pl.partial = want_partial || pl.splits > 1;
   pl.ncb = int(pl.partial ? N / kNB : ncb_fused);
+  pl.tc = pl.splits == 1 && tc_rows;
   return pl;
+}
+
+int launch_gemm(const GemmArgs &g, const GemmPlan &pl, cudaStream_t st) {
+  if (pl.tc && tc_supported(g) && (!pl.partial || g.act == MOE_ACT_NONE)) {
+    GemmArgs t = g;
+    if (pl.partial) {  // single split: the fp32 "partial" slice is the output itself
+      t.out = g.partial;
+      t.out_dtype = MOE_F32;
+    }
+    return launch_gemm_tc(t, st);
+  }
+  return launch_gemm_mma(g, pl, st);
 }
 
 int launch_gemm_mma(const GemmArgs &g, const GemmPlan &pl, cudaStream_t st) {

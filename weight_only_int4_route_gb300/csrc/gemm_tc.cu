@@ -1,0 +1,577 @@
+// Grouped GEMM on the 5th-generation tensor cores (tcgen05, TMEM accumulators) for experts
+// with many routed rows (prefill-sized batches).
+//
+// "Who Says Elephants Can't Run", section 3 / Figure 1: one launch computes every expert's
+// sub-matrix product; section 4: dequantization fused into the GEMM; optimized I2F with the
+// interleaved INT4 word.  "Specter", method step 5: tokens grouped per expert form a GEMM.
+//
+// Orientation (swap-AB): D[128 output channels x N rows] = W^T[128 x K] . Xp^T[K x N].
+//   * A operand = dequantized weights, written by dequant warps straight into tensor memory
+//     (tcgen05.st), never through shared memory: shared-memory bandwidth is left to the
+//     activation operand.
+//   * B operand = 128 consecutive rows of the expert's segment of Xp, TMA-loaded with
+//     128-byte swizzle (K-major), so the MMA reads it through a shared-memory descriptor.
+//   * D = fp32 accumulator in tensor memory, double-buffered so the epilogue of one tile
+//     overlaps the mainloop of the next.
+//
+// Warp roles (448 threads, one CTA per SM, persistent over tiles):
+//   warps 0-3   epilogue: tcgen05.ld of D, scale / activation, global stores;
+//   warp 4      producer: TMA of the packed weight block and the activation block;
+//   warp 5      MMA issuer (one thread);
+//   warps 6-13  dequant: warp w owns TMEM lanes 32*(w%4).. and one half of each 64-wide
+//               K block; reads its channel's packed words from shared memory, converts
+//               them with the magic-number I2F (and the group scale) and stores the pairs.
+// TMEM columns: [0,256) two 128-column accumulators, [256,512) eight 32-column A stages.
+//
+// Every wait on an mbarrier is bounded (about a second); on expiry the CTA records an
+// error code in a device word, stops issuing work, drains its own asynchronous copies and
+// MMAs, frees its tensor memory and returns.
+#include <cuda.h>
+
+#include <algorithm>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+
+__device__ int g_moe_device_error = 0;
+
+namespace {
+
+constexpr int kThreads = 448;
+constexpr int kBM = 128;          // output channels per tile (MMA M)
+constexpr int kBN = 128;          // rows per tile (MMA N upper bound)
+constexpr int kBK = 64;           // K per pipeline stage
+constexpr int kStages = 6;        // shared-memory stages
+constexpr int kAStages = 8;       // TMEM A stages
+constexpr int kMaxE = 256;
+constexpr int kBBytes = kBN * kBK * 2;       // activation stage: 16 KB
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kACol0 = 256;
+constexpr long long kTimeoutCycles = 4000000000LL;  // ~2 s at 2 GHz
+
+enum : int { kErrTimeoutFull = 1, kErrTimeoutEmpty = 2, kErrTimeoutA = 3, kErrTimeoutD = 4, kErrTimeoutDrain = 5 };
+
+template <int BITS> struct WB {
+  static constexpr int kWordsPerRow = kBK * BITS / 32;    // u32 words per channel per stage
+  static constexpr int kBytes = kBM * kWordsPerRow * 4;   // weight stage bytes
+};
+
+struct TcParams {
+  const int32_t *offsets;
+  const uint16_t *scales;
+  void *out;
+  int R, E, K, N, group, act, out_dtype, ncb, swiglu;
+};
+
+// ---------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t su32(const void *p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+
+__device__ __forceinline__ void mbar_init(uint64_t *b, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(su32(b)), "r"(count));
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(su32(b)) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(su32(b)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint64_t *b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(su32(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: false if the CTA aborted or this wait expired (then the abort flag is set).
+__device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity, volatile int *abort_flag, int code) {
+  if (mbar_try(b, parity)) return true;
+  const long long t0 = clock64();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try(b, parity)) return true;
+    if ((it & 63) == 0) {
+      if (*abort_flag) return false;
+      if (clock64() - t0 > kTimeoutCycles) {
+        *abort_flag = 1;
+        atomicExch(&g_moe_device_error, code);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::"r"(
+          su32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(su32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
+
+__device__ __forceinline__ void tc_commit(uint64_t *bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(su32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};\n" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
+
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15}, [%16];\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= uint64_t((saddr >> 4) & 0x3FFFu);          // start address
+  d |= uint64_t(1) << 16;                          // leading byte offset (unused with swizzle)
+  d |= uint64_t(1024 >> 4) << 32;                  // stride byte offset
+  d |= uint64_t(1) << 46;                          // descriptor version
+  d |= uint64_t(2) << 61;                          // SWIZZLE_128B
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 D, A/B f16 (0) or bf16 (1), both K-major.
+__host__ __device__ constexpr uint32_t idesc_f16(int is_bf16, int M, int N) {
+  return (1u << 4) | (uint32_t(is_bf16) << 7) | (uint32_t(is_bf16) << 10) | (uint32_t(N >> 3) << 17) |
+         (uint32_t(M >> 4) << 24);
+}
+
+template <typename T> __device__ __forceinline__ float ldscale(const uint16_t *s, int64_t i) {
+  const uint16_t b = s[i];
+  if constexpr (std::is_same<T, __half>::value) return __half2float(__ushort_as_half(b));
+  else return __bfloat162float(__ushort_as_bfloat16(b));
+}
+
+__device__ __forceinline__ void store_val(void *out, int dt, int64_t i, float v) {
+  if (dt == MOE_F32) static_cast<float *>(out)[i] = v;
+  else if (dt == MOE_F16) static_cast<__half *>(out)[i] = __float2half_rn(v);
+  else static_cast<__nv_bfloat16 *>(out)[i] = __float2bfloat16_rn(v);
+}
+
+struct Tile {
+  int e, row0, nrows, cb;
+};
+
+__device__ __forceinline__ Tile decode_tile(int tile, const int *s_tstart, const int *s_off, int E, int ncb) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_tstart[mid] <= tile) lo = mid;
+    else hi = mid - 1;
+  }
+  Tile t;
+  t.e = lo;
+  const int in_e = tile - s_tstart[lo];
+  const int tt = in_e / ncb;
+  t.cb = in_e - tt * ncb;
+  t.row0 = s_off[lo] + tt * kBN;
+  t.nrows = min(kBN, s_off[lo + 1] - t.row0);
+  return t;
+}
+
+template <typename T, int BITS>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
+                   const TcParams p) {
+  constexpr int kWBytes = WB<BITS>::kBytes;
+  constexpr int kWords = WB<BITS>::kWordsPerRow;
+  extern __shared__ __align__(1024) uint8_t dsmem[];
+  uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dsmem) + 1023) & ~uintptr_t(1023));
+  uint8_t *sB = base;                                   // kStages x 16 KB (1024-aligned)
+  uint8_t *sW = sB + kStages * kBBytes;                 // kStages x kWBytes
+  float *sX = reinterpret_cast<float *>(sW + kStages * kWBytes);  // SwiGLU exchange: 16 x 64 fp32
+  uint64_t *bar = reinterpret_cast<uint64_t *>(sX + 16 * 64);
+  uint64_t *full = bar, *empty = bar + kStages, *a_full = bar + 2 * kStages, *a_empty = a_full + kAStages;
+  uint64_t *d_full = a_empty + kAStages, *d_empty = d_full + 2, *drain = d_empty + 2;
+  int *s_tstart = reinterpret_cast<int *>(drain + 1);
+  int *s_off = s_tstart + kMaxE + 1;
+  int *scratch = s_off + kMaxE + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(scratch + 32);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int E = p.E;
+
+  // ---- setup: barriers, TMEM, tile table
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1 + 8);
+    }
+    for (int s = 0; s < kAStages; ++s) {
+      mbar_init(&a_full[s], 8);
+      mbar_init(&a_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&d_full[s], 1);
+      mbar_init(&d_empty[s], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(su32(tmem_slot)),
+                 "r"(kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::);
+  }
+  int cnt = 0;
+  if (tid < E) {
+    const int o0 = p.offsets[tid], o1 = p.offsets[tid + 1];
+    cnt = ((o1 - o0 + kBN - 1) / kBN) * p.ncb;
+    s_off[tid] = o0;
+    if (tid == E - 1) s_off[E] = o1;
+  }
+  int start = 0;
+  const int total_tiles = block_exclusive_scan(cnt, &start, scratch);  // contains __syncthreads
+  if (tid < E) s_tstart[tid] = start;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int nkb = p.K / kBK;
+  const int is_bf16 = std::is_same<T, __nv_bfloat16>::value ? 1 : 0;
+
+  if (warp == 4) {
+    // ------------------------------------------------ producer (TMA)
+    if (lane == 0) {
+      uint32_t it = 0;
+      int issued[kStages];
+#pragma unroll
+      for (int s = 0; s < kStages; ++s) issued[s] = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+        const Tile t = decode_tile(tile, s_tstart, s_off, E, p.ncb);
+        const int rowA = t.e * p.N + (p.swiglu ? t.cb * (kBM / 2) : t.cb * kBM);
+        const int rowB = p.swiglu ? t.e * p.N + (p.N >> 1) + t.cb * (kBM / 2) : rowA + kBM / 2;
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = it % kStages;
+          if (!mbar_wait(&empty[s], ((it / kStages) & 1) ^ 1, abort_flag, kErrTimeoutEmpty)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(&full[s], kBBytes + kWBytes);
+          tma_load_2d(sB + s * kBBytes, &map_x, kb * kBK, t.row0, &full[s]);
+          tma_load_2d(sW + s * kWBytes, &map_w, kb * kWords, rowA, &full[s]);
+          tma_load_2d(sW + s * kWBytes + kWBytes / 2, &map_w, kb * kWords, rowB, &full[s]);
+          issued[s] = int((it / kStages) & 1) + 1;  // parity of this fill, +1
+        }
+      }
+      // drain: every issued copy has landed before the CTA may exit
+#pragma unroll
+      for (int s = 0; s < kStages; ++s)
+        if (issued[s]) {
+          volatile int never = 0;
+          mbar_wait(&full[s], uint32_t(issued[s] - 1), &never, kErrTimeoutDrain);
+        }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t it = 0, ait = 0, tcount = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x, ++tcount) {
+        const Tile t = decode_tile(tile, s_tstart, s_off, E, p.ncb);
+        const int n = (t.nrows + 15) & ~15;
+        const uint32_t idesc = idesc_f16(is_bf16, kBM, n);
+        const int db = tcount & 1;
+        if (!mbar_wait(&d_empty[db], ((tcount >> 1) & 1) ^ 1, abort_flag, kErrTimeoutD)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + uint32_t(db * kBN);
+        for (int kb = 0; kb < nkb; ++kb, ++it, ++ait) {
+          const int s = it % kStages, as = ait % kAStages;
+          if (!mbar_wait(&full[s], (it / kStages) & 1, abort_flag, kErrTimeoutFull) ||
+              !mbar_wait(&a_full[as], (ait / kAStages) & 1, abort_flag, kErrTimeoutA)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t b_addr = su32(sB + s * kBBytes);
+#pragma unroll
+          for (int j = 0; j < kBK / 16; ++j) {
+            const uint64_t bd = sw128_desc(b_addr + j * 32);
+            tc_mma_ts(d_tmem, tmem + kACol0 + uint32_t(as * 32 + j * 8), bd, idesc, (kb | j) != 0);
+          }
+          tc_commit(&empty[s]);
+          tc_commit(&a_empty[as]);
+        }
+        if (ok) tc_commit(&d_full[db]);
+      }
+      // drain: all issued MMAs complete before TMEM is released
+      tc_commit(drain);
+      volatile int never = 0;
+      mbar_wait(drain, 0, &never, kErrTimeoutDrain);
+    }
+  } else if (warp >= 6) {
+    // ------------------------------------------------ dequant -> TMEM A stages
+    const int q = warp & 3;          // TMEM lane quarter
+    const int half = (warp - 6) >> 2;  // which 32-wide half of the 64-wide K block
+    const int r = q * 32 + lane;     // A row (channel within the tile)
+    uint32_t it = 0, ait = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+      const Tile t = decode_tile(tile, s_tstart, s_off, E, p.ncb);
+      int ch;
+      if (p.swiglu) ch = r < kBM / 2 ? t.cb * (kBM / 2) + r : (p.N >> 1) + t.cb * (kBM / 2) + (r - kBM / 2);
+      else ch = t.cb * kBM + r;
+      const int G = p.group == 0 ? 1 : p.K / p.group;
+      const uint16_t *srow = p.scales + int64_t(t.e) * G * p.N + ch;
+      for (int kb = 0; kb < nkb; ++kb, ++it, ++ait) {
+        const int s = it % kStages, as = ait % kAStages;
+        if (!mbar_wait(&full[s], (it / kStages) & 1, abort_flag, kErrTimeoutFull)) {
+          ok = false;
+          break;
+        }
+        // this lane's 32 reduction indices: words [half*kWords/2, +kWords/2) of row r
+        const uint8_t *wp = sW + s * kWBytes + r * (kWords * 4) + half * (kWords * 2);
+        uint32_t pr[16];
+        if constexpr (BITS == 4) {
+          const uint4 w = *reinterpret_cast<const uint4 *>(wp);
+          const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint32_t h[4];
+            i2f_int4(words[i], h, T());
+#pragma unroll
+            for (int j = 0; j < 4; ++j) pr[4 * i + j] = h[j];
+          }
+        } else {
+          const uint4 w0 = *reinterpret_cast<const uint4 *>(wp);
+          const uint4 w1 = *reinterpret_cast<const uint4 *>(wp + 16);
+          const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            uint32_t h[2];
+            i2f_int8(words[i], h, T());
+            pr[2 * i] = h[0];
+            pr[2 * i + 1] = h[1];
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        if (p.group != 0) {
+          const uint16_t sb = srow[int64_t((kb * kBK) / p.group) * p.N];
+          const uint32_t s2 = uint32_t(sb) | (uint32_t(sb) << 16);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) pr[j] = scale_pair(pr[j], s2, T());
+        }
+        if (!mbar_wait(&a_empty[as], ((ait / kAStages) & 1) ^ 1, abort_flag, kErrTimeoutA)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        tc_st16(tmem + (uint32_t(q * 32) << 16) + kACol0 + uint32_t(as * 32 + half * 16), pr);
+        tc_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&a_full[as]);
+      }
+    }
+  } else {
+    // ------------------------------------------------ epilogue (warps 0-3)
+    const int q = warp;
+    const int r = q * 32 + lane;
+    uint32_t tcount = 0;
+    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++tcount) {
+      const Tile t = decode_tile(tile, s_tstart, s_off, E, p.ncb);
+      const int db = tcount & 1;
+      if (!mbar_wait(&d_full[db], (tcount >> 1) & 1, abort_flag, kErrTimeoutD)) break;
+      tc_fence_after();
+      int ch;
+      if (p.swiglu) ch = r < kBM / 2 ? t.cb * (kBM / 2) + r : (p.N >> 1) + t.cb * (kBM / 2) + (r - kBM / 2);
+      else ch = t.cb * kBM + r;
+      const float sc = p.group == 0 ? ldscale<T>(p.scales, int64_t(t.e) * p.N + ch) : 1.0f;
+      const int Nout = p.swiglu ? (p.N >> 1) : p.N;
+      for (int c0 = 0; c0 < t.nrows; c0 += 16) {
+        float v[16];
+        tc_ld16(tmem + (uint32_t(q * 32) << 16) + uint32_t(db * kBN + c0), v);
+        if (p.swiglu) {
+          // up rows (quarters 2,3) hand their values to the gate rows (quarters 0,1)
+          if (q >= 2) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) sX[j * 64 + (r - 64)] = v[j] * sc;
+          }
+          asm volatile("bar.sync 1, 128;\n" ::: "memory");
+          if (q < 2) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int row = c0 + j;
+              if (row < t.nrows) {
+                const float g = v[j] * sc;
+                store_val(p.out, p.out_dtype, int64_t(t.row0 + row) * Nout + t.cb * (kBM / 2) + r,
+                          act_silu(g) * sX[j * 64 + r]);
+              }
+            }
+          }
+          asm volatile("bar.sync 1, 128;\n" ::: "memory");
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int row = c0 + j;
+            if (row < t.nrows)
+              store_val(p.out, p.out_dtype, int64_t(t.row0 + row) * Nout + ch, act_apply(v[j] * sc, p.act));
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&d_empty[db]);
+    }
+  }
+
+  // ---- teardown: everyone done, release tensor memory
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kTmemCols));
+}
+
+// ---------------------------------------------------------------- host side
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+size_t smem_bytes(int bits) {
+  const size_t wbytes = bits == 4 ? WB<4>::kBytes : WB<8>::kBytes;
+  return 1024 /*align slack*/ + kStages * (kBBytes + wbytes) + 16 * 64 * 4 + (2 * kStages + 2 * kAStages + 5) * 8 +
+         (2 * (kMaxE + 1) + 32 + 2) * 4;
+}
+
+template <typename T, int BITS>
+int launch_typed(const GemmArgs &g, cudaStream_t st) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return set_error(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  CUtensorMap mx, mw;
+  {
+    const cuuint64_t dims[2] = {cuuint64_t(g.K), cuuint64_t(g.R)};
+    const cuuint64_t strides[1] = {cuuint64_t(g.K) * 2};
+    const cuuint32_t box[2] = {cuuint32_t(kBK), cuuint32_t(kBN)};
+    const cuuint32_t es[2] = {1, 1};
+    const CUresult r = enc(&mx, std::is_same<T, __half>::value ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                           2, const_cast<void *>(g.a), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return set_error(MOE_ERR_CUDA, "activation tensor map encode failed (%d)", int(r));
+  }
+  {
+    const int words_per_row = g.K * BITS / 32;
+    const cuuint64_t dims[2] = {cuuint64_t(words_per_row), cuuint64_t(int64_t(g.E) * g.N)};
+    const cuuint64_t strides[1] = {cuuint64_t(words_per_row) * 4};
+    const cuuint32_t box[2] = {cuuint32_t(WB<BITS>::kWordsPerRow), cuuint32_t(kBM / 2)};
+    const cuuint32_t es[2] = {1, 1};
+    const CUresult r = enc(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(g.w), dims, strides, box, es,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return set_error(MOE_ERR_CUDA, "weight tensor map encode failed (%d)", int(r));
+  }
+  TcParams tp{};
+  tp.offsets = g.offsets;
+  tp.scales = static_cast<const uint16_t *>(g.scales);
+  tp.out = g.out;
+  tp.R = int(g.R);
+  tp.E = g.E;
+  tp.K = g.K;
+  tp.N = g.N;
+  tp.group = g.group;
+  tp.act = g.act;
+  tp.out_dtype = g.out_dtype;
+  tp.swiglu = g.act == MOE_ACT_SWIGLU ? 1 : 0;
+  tp.ncb = tp.swiglu ? g.N / kBM : g.N / kBM;  // SwiGLU: 64 gate + 64 up channels per tile
+  const size_t smem = smem_bytes(BITS);
+  static bool attr_set[2][2] = {{false, false}, {false, false}};
+  bool &done = attr_set[std::is_same<T, __half>::value ? 0 : 1][BITS == 4 ? 0 : 1];
+  if (!done) {
+    if (cudaFuncSetAttribute(gemm_tc_kernel<T, BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
+        cudaSuccess)
+      return check_launch("gemm_tc attribute");
+    done = true;
+  }
+  // tiles upper bound: (row tiles) x channel blocks
+  const int64_t row_tiles = std::min<int64_t>(g.E, g.R) + cdiv(g.R, kBN);
+  const int64_t tiles = row_tiles * tp.ncb;
+  const int grid = int(std::max<int64_t>(1, std::min<int64_t>(tiles, num_sms())));
+  gemm_tc_kernel<T, BITS><<<grid, kThreads, smem, st>>>(mx, mw, tp);
+  return check_launch("grouped_gemm_tc");
+}
+
+}  // namespace
+
+bool tc_supported(const GemmArgs &g) {
+  if (g.bits != 4 && g.bits != 8) return false;
+  if (g.offsets == nullptr) return false;
+  if (g.K % kBK != 0) return false;
+  if (g.act == MOE_ACT_SWIGLU) {
+    if ((g.N / 2) % (kBM / 2) != 0) return false;
+  } else if (g.N % kBM != 0) {
+    return false;
+  }
+  if (g.group != 0 && g.group % kBK != 0) return false;
+  if (int64_t(g.E) * g.N >= (int64_t(1) << 31)) return false;
+  return true;
+}
+
+int launch_gemm_tc(const GemmArgs &g, cudaStream_t st) {
+  if (g.R == 0) return MOE_OK;
+  const bool bf = g.a_dtype == MOE_BF16;
+  if (g.bits == 4) return bf ? launch_typed<__nv_bfloat16, 4>(g, st) : launch_typed<__half, 4>(g, st);
+  return bf ? launch_typed<__nv_bfloat16, 8>(g, st) : launch_typed<__half, 8>(g, st);
+}
+
+int read_device_error(cudaStream_t st, int *out) {
+  if (cudaStreamSynchronize(st) != cudaSuccess) return check_launch("device error read");
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_moe_device_error, sizeof(int)) != cudaSuccess) return check_launch("device error read");
+  const int zero = 0;
+  if (cudaMemcpyToSymbol(g_moe_device_error, &zero, sizeof(int)) != cudaSuccess) return check_launch("device error reset");
+  *out = v;
+  return MOE_OK;
+}
+
+}  // namespace moe

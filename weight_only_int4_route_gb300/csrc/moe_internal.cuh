@@ -49,6 +49,7 @@ struct GemmPlan {
   int ks;      // K per split (multiple of 128)
   int ncb;     // channel blocks
   bool partial;  // fp32 partial slices instead of the fused epilogue
+  bool tc;       // rows per active expert large enough for the tcgen05 path
 };
 GemmPlan plan_gemm(int64_t R, int64_t E, int64_t K, int64_t N, int act, bool want_partial);
 
@@ -68,8 +69,13 @@ struct GemmArgs {
   int bits;
 };
 // Enqueue the grouped GEMM described by `g` with plan `pl`.  When pl.partial, the fp32
-// accumulators (times per-channel scales) go to g.partial (splits, R, N).
+// accumulators (times per-channel scales) go to g.partial (splits, R, N).  Dispatches to the
+// tcgen05 kernel when the plan and the shapes allow it, else to the warp-MMA kernel.
+int launch_gemm(const GemmArgs &g, const GemmPlan &pl, cudaStream_t st);
 int launch_gemm_mma(const GemmArgs &g, const GemmPlan &pl, cudaStream_t st);
+bool tc_supported(const GemmArgs &g);
+int launch_gemm_tc(const GemmArgs &g, cudaStream_t st);
+int read_device_error(cudaStream_t st, int *out);
 // out[r, c] = act(sum_s part[s, r, c]) (SWIGLU pairs column c with c + N/2).
 int launch_reduce_act(const float *part, int splits, int64_t R, int N, int act, void *out,
                       int out_dtype, cudaStream_t st);

@@ -51,6 +51,7 @@ class LayerRouting(ctypes.Structure):
 _SIGS = {
     "moe_last_error_string": (ctypes.c_char_p, []),
     "moe_version": (_c_int, []),
+    "moe_device_error": (_c_int, [_vp, ctypes.POINTER(ctypes.c_int32)]),
     "moe_packed_size": (_c_size, [_c_i64, _c_i64, _c_i64, _c_int, _c_int]),
     "moe_packed_scale_offset": (_c_size, [_c_i64, _c_i64, _c_i64, _c_int]),
     "moe_pack_weights": (_c_int, [_vp, _vp, _c_int, _c_i64, _c_i64, _c_i64, _c_int, _c_int, _vp, _c_size, _vp]),
@@ -58,6 +59,7 @@ _SIGS = {
     "moe_route_topk": (_c_int, [_vp, _c_int, _vp, _c_int, _vp, _c_i64, _c_i64, _c_i64, _c_int, _c_int, _vp, _vp, _vp]),
     "moe_permute_workspace_size": (_c_size, [_c_i64, _c_i64, _c_int]),
     "moe_permute": (_c_int, [_vp, _vp, _c_int, _c_i64, _c_i64, _c_i64, _c_int, _vp, _vp, _vp, _vp, _vp, _c_size, _vp]),
+    "moe_gemm_path": (_c_int, [_c_i64, _c_i64, _c_i64, _c_i64, _c_int, _c_int, _c_int]),
     "moe_grouped_gemm_workspace_size": (_c_size, [_c_i64, _c_i64, _c_i64, _c_i64, _c_int, _c_int]),
     "moe_grouped_gemm_w4a16": (_c_int, [_vp, _c_int, _vp, _c_i64, _c_i64, _c_i64, _c_int, _vp, _c_i64, _c_int, _vp, _c_int, _vp, _c_size, _vp]),
     "moe_grouped_gemm_w8a16": (_c_int, [_vp, _c_int, _vp, _c_i64, _c_i64, _c_i64, _c_int, _vp, _c_i64, _c_int, _vp, _c_int, _vp, _c_size, _vp]),
@@ -115,6 +117,13 @@ def _stream(device: torch.device):
 
 def _dt(t: torch.Tensor) -> int:
     return _TORCH2MOE[t.dtype]
+
+
+def device_error(device="cuda:0") -> int:
+    """Synchronize the current stream and return (and clear) the library's device error code."""
+    v = ctypes.c_int32(0)
+    _check(lib().moe_device_error(_stream(torch.device(device)), ctypes.byref(v)), "moe_device_error")
+    return int(v.value)
 
 
 # ---------------------------------------------------------------- weights
@@ -191,6 +200,11 @@ def grouped_gemm(a: torch.Tensor, packed: torch.Tensor, bits: int, E: int, K: in
         st = lib().moe_grouped_gemm_w16a16(*args, *tail)
     _check(st, f"moe_grouped_gemm (bits {bits})")
     return out
+
+
+def gemm_path(R, E, K, N, bits, group, act: str) -> str:
+    """'tcgen05' or 'mma': the kernel a grouped GEMM of this shape dispatches to."""
+    return "tcgen05" if lib().moe_gemm_path(R, E, K, N, bits, group, ACT[act]) == 1 else "mma"
 
 
 def unpermute_combine(yp: torch.Tensor, inv_perm: torch.Tensor, gate: torch.Tensor,
