@@ -14,16 +14,25 @@
 //   * D = fp32 accumulator in tensor memory, double-buffered so the epilogue of one tile
 //     overlaps the mainloop of the next.
 //
-// Warp roles (448 threads, one CTA per SM, persistent over tiles):
-//   warps 0-3   epilogue: tcgen05.ld of D, scale / activation, global stores;
-//   warp 4      producer: TMA of the packed weight block and the activation block;
-//   warp 5      MMA issuer (one thread);
-//   warps 6-13  dequant: warp w owns TMEM lanes 32*(w%4).. and one half of each 64-wide
-//               K block; reads its channel's packed words from shared memory, converts
-//               them with the magic-number I2F (and the group scale) and stores the pairs.
-// TMEM columns: [0,256) two 128-column accumulators, [256,512) eight 32-column A stages.
+// Warp roles (one CTA per SM, persistent over tiles):
+//   warps 0-7    epilogue: warp w reads TMEM lanes 32*(w%4).. and one half of the tile's
+//                columns; scale / activation, global stores;
+//   warp 8       producer: TMA of the packed weight block and the activation block;
+//   warp 9       MMA issuer (one thread);
+//   warps 10-21  dequant, three groups of four warps; group g converts the K blocks with
+//                index = g (mod 3).  Warp w owns TMEM lanes 32*(w%4).. (one output channel
+//                per lane); it reads that channel's packed words from shared memory,
+//                converts them with the magic-number I2F (and the group-128 scale) and
+//                stores the 16-bit pairs into the A stage.
+// TMEM columns: [0,256) two 128-column accumulators, [256,512) four 64-column A stages.
 //
-// Every wait on an mbarrier is bounded (about a second); on expiry the CTA records an
+// Synchronisation per 128-wide K block: the producer's TMA completes `full`; the dequant
+// group waits on it, fills the TMEM A stage and arrives on `ready`; the MMA thread waits
+// only on `ready` (the data behind it was seen complete by the dequant warps) and issues
+// eight MMAs; one commit on `free` releases both the shared-memory stage and the A stage.
+// A K block of 128 keeps 512 tensor cycles of work queued behind each wait/commit pair.
+//
+// Every wait on an mbarrier is bounded (about two seconds); on expiry the CTA records an
 // error code in a device word, stops issuing work, drains its own asynchronous copies and
 // MMAs, frees its tensor memory and returns.
 #include <cuda.h>
@@ -38,19 +47,23 @@ __device__ int g_moe_device_error = 0;
 
 namespace {
 
-constexpr int kThreads = 448;
+constexpr int kEpiWarps = 8;        // epilogue warps (two per TMEM lane quarter)
+constexpr int kDqGroups = 3;        // dequant warp groups (each: 4 warps covering 128 lanes)
+constexpr int kProdWarp = kEpiWarps, kMmaWarp = kEpiWarps + 1, kDqWarp0 = kEpiWarps + 2;
+constexpr int kThreads = (kDqWarp0 + 4 * kDqGroups) * 32;
 constexpr int kBM = 128;          // output channels per tile (MMA M)
 constexpr int kBN = 128;          // rows per tile (MMA N upper bound)
-constexpr int kBK = 64;           // K per pipeline stage
-constexpr int kStages = 6;        // shared-memory stages
-constexpr int kAStages = 8;       // TMEM A stages
+constexpr int kBK = 128;          // K per pipeline stage
+constexpr int kStages = 4;        // pipeline stages (shared memory and TMEM A)
 constexpr int kMaxE = 256;
-constexpr int kBBytes = kBN * kBK * 2;       // activation stage: 16 KB
+constexpr int kBHalf = kBN * 64 * 2;         // one 64-wide swizzle atom column block: 16 KB
+constexpr int kBBytes = 2 * kBHalf;          // activation stage: 32 KB
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kACol0 = 256;
+constexpr uint32_t kAStageCols = kBK / 2;    // 64 columns of 16-bit pairs
 constexpr long long kTimeoutCycles = 4000000000LL;  // ~2 s at 2 GHz
 
-enum : int { kErrTimeoutFull = 1, kErrTimeoutEmpty = 2, kErrTimeoutA = 3, kErrTimeoutD = 4, kErrTimeoutDrain = 5 };
+enum : int { kErrTimeoutFull = 1, kErrTimeoutFree = 2, kErrTimeoutReady = 3, kErrTimeoutD = 4, kErrTimeoutDrain = 5 };
 
 template <int BITS> struct WB {
   static constexpr int kWordsPerRow = kBK * BITS / 32;    // u32 words per channel per stage
@@ -151,6 +164,22 @@ __device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 bytes apart.
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   uint64_t d = 0;
@@ -201,6 +230,58 @@ __device__ __forceinline__ Tile decode_tile(int tile, const int *s_tstart, const
   return t;
 }
 
+template <typename OT> __device__ __forceinline__ void store_typed(void *out, int64_t i, float v) {
+  static_cast<OT *>(out)[i] = from_f32<OT>(v);
+}
+
+// Epilogue of one tile for one warp: TMEM lanes 32q.. (output channel rows), tile columns
+// [c_lo, c_hi) (routed rows).  SwiGLU tiles hold 64 gate rows then the 64 matching up rows;
+// the up quarters hand their values to the gate quarters through shared memory.
+template <typename T, typename OT>
+__device__ __forceinline__ void epilogue_cols(const TcParams &p, const Tile &t, uint32_t tmem_d, int q, int lane,
+                                              int c_lo, int c_hi, float *xbuf, int bar_id) {
+  const int r = q * 32 + lane;
+  int ch;
+  if (p.swiglu) ch = r < kBM / 2 ? t.cb * (kBM / 2) + r : (p.N >> 1) + t.cb * (kBM / 2) + (r - kBM / 2);
+  else ch = t.cb * kBM + r;
+  const float sc = p.group == 0 ? ldscale<T>(p.scales, int64_t(t.e) * p.N + ch) : 1.0f;
+  const int Nout = p.swiglu ? (p.N >> 1) : p.N;
+  for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
+    float v[32];
+    tc_ld32(tmem_d + (uint32_t(q * 32) << 16) + uint32_t(c0), v);
+    const int nvalid = min(32, t.nrows - c0);
+    if (p.swiglu) {
+      if (q >= 2) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) xbuf[j * 64 + (r - 64)] = v[j] * sc;
+      }
+      asm volatile("bar.sync %0, 128;\n" ::"r"(bar_id) : "memory");
+      if (q < 2) {
+        OT *o = static_cast<OT *>(p.out) + int64_t(t.row0 + c0) * Nout + t.cb * (kBM / 2) + r;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j < nvalid) o[int64_t(j) * Nout] = from_f32<OT>(act_silu(v[j] * sc) * xbuf[j * 64 + r]);
+      }
+      asm volatile("bar.sync %0, 128;\n" ::"r"(bar_id) : "memory");
+    } else {
+      OT *o = static_cast<OT *>(p.out) + int64_t(t.row0 + c0) * Nout + ch;
+      if (p.act == MOE_ACT_GELU) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j < nvalid) o[int64_t(j) * Nout] = from_f32<OT>(act_gelu(v[j] * sc));
+      } else if (p.act == MOE_ACT_RELU) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j < nvalid) o[int64_t(j) * Nout] = from_f32<OT>(act_relu(v[j] * sc));
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j < nvalid) o[int64_t(j) * Nout] = from_f32<OT>(v[j] * sc);
+      }
+    }
+  }
+}
+
 template <typename T, int BITS>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
@@ -209,12 +290,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kWords = WB<BITS>::kWordsPerRow;
   extern __shared__ __align__(1024) uint8_t dsmem[];
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dsmem) + 1023) & ~uintptr_t(1023));
-  uint8_t *sB = base;                                   // kStages x 16 KB (1024-aligned)
+  uint8_t *sB = base;                                   // kStages x 32 KB (two 1024-aligned 16 KB halves)
   uint8_t *sW = sB + kStages * kBBytes;                 // kStages x kWBytes
-  float *sX = reinterpret_cast<float *>(sW + kStages * kWBytes);  // SwiGLU exchange: 16 x 64 fp32
-  uint64_t *bar = reinterpret_cast<uint64_t *>(sX + 16 * 64);
-  uint64_t *full = bar, *empty = bar + kStages, *a_full = bar + 2 * kStages, *a_empty = a_full + kAStages;
-  uint64_t *d_full = a_empty + kAStages, *d_empty = d_full + 2, *drain = d_empty + 2;
+  float *sX = reinterpret_cast<float *>(sW + kStages * kWBytes);  // SwiGLU exchange: 2 halves x 32 x 64 fp32
+  uint64_t *bar = reinterpret_cast<uint64_t *>(sX + 2 * 32 * 64);
+  uint64_t *full = bar, *ready = bar + kStages, *freeb = bar + 2 * kStages;
+  uint64_t *d_full = bar + 3 * kStages, *d_empty = d_full + 2, *drain = d_empty + 2;
   int *s_tstart = reinterpret_cast<int *>(drain + 1);
   int *s_off = s_tstart + kMaxE + 1;
   int *scratch = s_off + kMaxE + 1;
@@ -228,15 +309,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1 + 8);
-    }
-    for (int s = 0; s < kAStages; ++s) {
-      mbar_init(&a_full[s], 8);
-      mbar_init(&a_empty[s], 1);
+      mbar_init(&ready[s], 4);
+      mbar_init(&freeb[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&d_full[s], 1);
-      mbar_init(&d_empty[s], 4);
+      mbar_init(&d_empty[s], kEpiWarps);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -264,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nkb = p.K / kBK;
   const int is_bf16 = std::is_same<T, __nv_bfloat16>::value ? 1 : 0;
 
-  if (warp == 4) {
+  if (warp == kProdWarp) {
     // ------------------------------------------------ producer (TMA)
     if (lane == 0) {
       uint32_t it = 0;
@@ -278,12 +356,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int rowB = p.swiglu ? t.e * p.N + (p.N >> 1) + t.cb * (kBM / 2) : rowA + kBM / 2;
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % kStages;
-          if (!mbar_wait(&empty[s], ((it / kStages) & 1) ^ 1, abort_flag, kErrTimeoutEmpty)) {
+          if (!mbar_wait(&freeb[s], ((it / kStages) & 1) ^ 1, abort_flag, kErrTimeoutFree)) {
             ok = false;
             break;
           }
           mbar_expect_tx(&full[s], kBBytes + kWBytes);
           tma_load_2d(sB + s * kBBytes, &map_x, kb * kBK, t.row0, &full[s]);
+          tma_load_2d(sB + s * kBBytes + kBHalf, &map_x, kb * kBK + 64, t.row0, &full[s]);
           tma_load_2d(sW + s * kWBytes, &map_w, kb * kWords, rowA, &full[s]);
           tma_load_2d(sW + s * kWBytes + kWBytes / 2, &map_w, kb * kWords, rowB, &full[s]);
           issued[s] = int((it / kStages) & 1) + 1;  // parity of this fill, +1
@@ -297,10 +376,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_wait(&full[s], uint32_t(issued[s] - 1), &never, kErrTimeoutDrain);
         }
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
-      uint32_t it = 0, ait = 0, tcount = 0;
+      uint32_t it = 0, tcount = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x, ++tcount) {
         const Tile t = decode_tile(tile, s_tstart, s_off, E, p.ncb);
@@ -310,22 +389,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&d_empty[db], ((tcount >> 1) & 1) ^ 1, abort_flag, kErrTimeoutD)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + uint32_t(db * kBN);
-        for (int kb = 0; kb < nkb; ++kb, ++it, ++ait) {
-          const int s = it % kStages, as = ait % kAStages;
-          if (!mbar_wait(&full[s], (it / kStages) & 1, abort_flag, kErrTimeoutFull) ||
-              !mbar_wait(&a_full[as], (ait / kAStages) & 1, abort_flag, kErrTimeoutA)) {
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = it % kStages;
+          if (!mbar_wait(&ready[s], (it / kStages) & 1, abort_flag, kErrTimeoutReady)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t b_addr = su32(sB + s * kBBytes);
+          const uint32_t a_col = tmem + kACol0 + uint32_t(s) * kAStageCols;
 #pragma unroll
           for (int j = 0; j < kBK / 16; ++j) {
-            const uint64_t bd = sw128_desc(b_addr + j * 32);
-            tc_mma_ts(d_tmem, tmem + kACol0 + uint32_t(as * 32 + j * 8), bd, idesc, (kb | j) != 0);
+            const uint64_t bd = sw128_desc(b_addr + (j >> 2) * kBHalf + (j & 3) * 32);
+            tc_mma_ts(d_tmem, a_col + uint32_t(j * 8), bd, idesc, (kb | j) != 0);
           }
-          tc_commit(&empty[s]);
-          tc_commit(&a_empty[as]);
+          tc_commit(&freeb[s]);
         }
         if (ok) tc_commit(&d_full[db]);
       }
@@ -334,12 +412,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       volatile int never = 0;
       mbar_wait(drain, 0, &never, kErrTimeoutDrain);
     }
-  } else if (warp >= 6) {
+  } else if (warp >= kDqWarp0) {
     // ------------------------------------------------ dequant -> TMEM A stages
-    const int q = warp & 3;          // TMEM lane quarter
-    const int half = (warp - 6) >> 2;  // which 32-wide half of the 64-wide K block
-    const int r = q * 32 + lane;     // A row (channel within the tile)
-    uint32_t it = 0, ait = 0;
+    const int q = warp & 3;                  // TMEM lane quarter
+    const int grp = (warp - kDqWarp0) >> 2;  // converts K blocks kb with kb % kDqGroups == grp
+    const int r = q * 32 + lane;             // A row (channel within the tile)
+    uint32_t it = 0;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
       const Tile t = decode_tile(tile, s_tstart, s_off, E, p.ncb);
@@ -348,102 +426,83 @@ __global__ void __launch_bounds__(kThreads, 1)
       else ch = t.cb * kBM + r;
       const int G = p.group == 0 ? 1 : p.K / p.group;
       const uint16_t *srow = p.scales + int64_t(t.e) * G * p.N + ch;
-      for (int kb = 0; kb < nkb; ++kb, ++it, ++ait) {
-        const int s = it % kStages, as = ait % kAStages;
+      for (int kb = 0; kb < nkb; ++kb, ++it) {
+        if ((it % kDqGroups) != uint32_t(grp)) continue;
+        const int s = it % kStages;
+        uint32_t s2 = 0;
+        if (p.group != 0) {  // one scale per 128-wide K block (group 128)
+          const uint16_t sb = srow[int64_t((kb * kBK) / p.group) * p.N];
+          s2 = uint32_t(sb) | (uint32_t(sb) << 16);
+        }
         if (!mbar_wait(&full[s], (it / kStages) & 1, abort_flag, kErrTimeoutFull)) {
           ok = false;
           break;
         }
-        // this lane's 32 reduction indices: words [half*kWords/2, +kWords/2) of row r
-        const uint8_t *wp = sW + s * kWBytes + r * (kWords * 4) + half * (kWords * 2);
-        uint32_t pr[16];
-        if constexpr (BITS == 4) {
-          const uint4 w = *reinterpret_cast<const uint4 *>(wp);
-          const uint32_t words[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            uint32_t h[4];
-            i2f_int4(words[i], h, T());
-#pragma unroll
-            for (int j = 0; j < 4; ++j) pr[4 * i + j] = h[j];
-          }
-        } else {
-          const uint4 w0 = *reinterpret_cast<const uint4 *>(wp);
-          const uint4 w1 = *reinterpret_cast<const uint4 *>(wp + 16);
-          const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            uint32_t h[2];
-            i2f_int8(words[i], h, T());
-            pr[2 * i] = h[0];
-            pr[2 * i + 1] = h[1];
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
-        if (p.group != 0) {
-          const uint16_t sb = srow[int64_t((kb * kBK) / p.group) * p.N];
-          const uint32_t s2 = uint32_t(sb) | (uint32_t(sb) << 16);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) pr[j] = scale_pair(pr[j], s2, T());
-        }
-        if (!mbar_wait(&a_empty[as], ((ait / kAStages) & 1) ^ 1, abort_flag, kErrTimeoutA)) {
-          ok = false;
-          break;
-        }
         tc_fence_after();
-        tc_st16(tmem + (uint32_t(q * 32) << 16) + kACol0 + uint32_t(as * 32 + half * 16), pr);
+        const uint8_t *wp = sW + s * kWBytes + r * (kWords * 4);
+        const uint32_t ta = tmem + (uint32_t(q * 32) << 16) + kACol0 + uint32_t(s) * kAStageCols;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {   // two 64-wide halves of the K block, 32 columns each
+          uint32_t pr[32];
+          if constexpr (BITS == 4) {
+            const uint4 w0 = *reinterpret_cast<const uint4 *>(wp + 32 * h);
+            const uint4 w1 = *reinterpret_cast<const uint4 *>(wp + 32 * h + 16);
+            const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              uint32_t hh[4];
+              i2f_int4(words[i], hh, T());
+#pragma unroll
+              for (int j = 0; j < 4; ++j) pr[4 * i + j] = hh[j];
+            }
+          } else {
+            uint32_t words[16];
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const uint4 w = *reinterpret_cast<const uint4 *>(wp + 64 * h + 16 * v);
+              words[4 * v] = w.x;
+              words[4 * v + 1] = w.y;
+              words[4 * v + 2] = w.z;
+              words[4 * v + 3] = w.w;
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              uint32_t hh[2];
+              i2f_int8(words[i], hh, T());
+              pr[2 * i] = hh[0];
+              pr[2 * i + 1] = hh[1];
+            }
+          }
+          if (p.group != 0) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) pr[j] = scale_pair(pr[j], s2, T());
+          }
+          tc_st16(ta + uint32_t(32 * h), *reinterpret_cast<const uint32_t(*)[16]>(&pr[0]));
+          tc_st16(ta + uint32_t(32 * h + 16), *reinterpret_cast<const uint32_t(*)[16]>(&pr[16]));
+        }
         tc_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&a_full[as]);
+        if (lane == 0) mbar_arrive(&ready[s]);
       }
     }
   } else {
-    // ------------------------------------------------ epilogue (warps 0-3)
-    const int q = warp;
-    const int r = q * 32 + lane;
+    // ------------------------------------------------ epilogue (warps 0-7)
+    const int q = warp & 3;
+    const int half = warp >> 2;   // tile columns [64*half, 64*half + 64)
     uint32_t tcount = 0;
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++tcount) {
       const Tile t = decode_tile(tile, s_tstart, s_off, E, p.ncb);
       const int db = tcount & 1;
       if (!mbar_wait(&d_full[db], (tcount >> 1) & 1, abort_flag, kErrTimeoutD)) break;
       tc_fence_after();
-      int ch;
-      if (p.swiglu) ch = r < kBM / 2 ? t.cb * (kBM / 2) + r : (p.N >> 1) + t.cb * (kBM / 2) + (r - kBM / 2);
-      else ch = t.cb * kBM + r;
-      const float sc = p.group == 0 ? ldscale<T>(p.scales, int64_t(t.e) * p.N + ch) : 1.0f;
-      const int Nout = p.swiglu ? (p.N >> 1) : p.N;
-      for (int c0 = 0; c0 < t.nrows; c0 += 16) {
-        float v[16];
-        tc_ld16(tmem + (uint32_t(q * 32) << 16) + uint32_t(db * kBN + c0), v);
-        if (p.swiglu) {
-          // up rows (quarters 2,3) hand their values to the gate rows (quarters 0,1)
-          if (q >= 2) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) sX[j * 64 + (r - 64)] = v[j] * sc;
-          }
-          asm volatile("bar.sync 1, 128;\n" ::: "memory");
-          if (q < 2) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int row = c0 + j;
-              if (row < t.nrows) {
-                const float g = v[j] * sc;
-                store_val(p.out, p.out_dtype, int64_t(t.row0 + row) * Nout + t.cb * (kBM / 2) + r,
-                          act_silu(g) * sX[j * 64 + r]);
-              }
-            }
-          }
-          asm volatile("bar.sync 1, 128;\n" ::: "memory");
-        } else {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int row = c0 + j;
-            if (row < t.nrows)
-              store_val(p.out, p.out_dtype, int64_t(t.row0 + row) * Nout + ch, act_apply(v[j] * sc, p.act));
-          }
-        }
+      const int c_lo = 64 * half, c_hi = min(64 * half + 64, t.nrows);
+      const uint32_t tmem_d = tmem + uint32_t(db * kBN);
+      float *xbuf = sX + half * (32 * 64);
+      if (c_lo < c_hi) {
+        if (p.out_dtype == MOE_F32) epilogue_cols<T, float>(p, t, tmem_d, q, lane, c_lo, c_hi, xbuf, 1 + half);
+        else if (p.out_dtype == MOE_F16) epilogue_cols<T, __half>(p, t, tmem_d, q, lane, c_lo, c_hi, xbuf, 1 + half);
+        else epilogue_cols<T, __nv_bfloat16>(p, t, tmem_d, q, lane, c_lo, c_hi, xbuf, 1 + half);
       }
       tc_fence_before();
       __syncwarp();
@@ -481,7 +540,7 @@ EncodeTiledFn encode_fn() {
 
 size_t smem_bytes(int bits) {
   const size_t wbytes = bits == 4 ? WB<4>::kBytes : WB<8>::kBytes;
-  return 1024 /*align slack*/ + kStages * (kBBytes + wbytes) + 16 * 64 * 4 + (2 * kStages + 2 * kAStages + 5) * 8 +
+  return 1024 /*align slack*/ + kStages * (kBBytes + wbytes) + 2 * 32 * 64 * 4 + (3 * kStages + 5) * 8 +
          (2 * (kMaxE + 1) + 32 + 2) * 4;
 }
 
@@ -493,7 +552,7 @@ int launch_typed(const GemmArgs &g, cudaStream_t st) {
   {
     const cuuint64_t dims[2] = {cuuint64_t(g.K), cuuint64_t(g.R)};
     const cuuint64_t strides[1] = {cuuint64_t(g.K) * 2};
-    const cuuint32_t box[2] = {cuuint32_t(kBK), cuuint32_t(kBN)};
+    const cuuint32_t box[2] = {64u, cuuint32_t(kBN)};  // one 128-byte swizzle atom column block
     const cuuint32_t es[2] = {1, 1};
     const CUresult r = enc(&mx, std::is_same<T, __half>::value ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                            2, const_cast<void *>(g.a), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
