@@ -172,6 +172,23 @@ int moe_grouped_gemm_w8a16(const void *a, int a_dtype, const void *packed_w, int
                            int64_t N, int group, const int32_t *offsets, int64_t R, int act,
                            void *out, int out_dtype, void *workspace, size_t workspace_bytes,
                            moe_stream_t stream);
+/* moe_grouped_gemm_w4a16 for callers that cannot allocate device memory.  The pages have no
+ * counterpart to this call: it exists for callers whose device memory is owned by someone else
+ * (a runtime that pools all memory at start-up, a host framework that hands plug-ins only their
+ * inputs and outputs) or that must not call cudaMalloc while a stream is being captured.
+ * Same arguments and results as moe_grouped_gemm_w4a16 minus the workspace: the split-K
+ * partial sums go to a 2 MiB array inside the library (a file-scope __device__ variable that
+ * every GPU loading the library holds until exit).  Calls needing more scratch than that
+ * (moe_grouped_gemm_workspace_size > 2 MiB) return MOE_ERR_UNSUPPORTED without launching.
+ * Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.  The first call on
+ * a device looks up the array's device address (cudaGetSymbolAddress) with that device
+ * current; make that first call before any stream capture.  Every call on a device shares the
+ * one array and leaves its last contents there (each call overwrites every partial it reads,
+ * so nothing needs clearing); calls that overlap on the GPU (different streams, or several
+ * host threads) race on it and must be serialized by the caller. */
+int moe_grouped_gemm_w4a16_static(const void *a, int a_dtype, const void *packed_w, int64_t E,
+                                  int64_t K, int64_t N, int group, const int32_t *offsets, int64_t R,
+                                  int act, void *out, int out_dtype, moe_stream_t stream);
 /* Unquantized 16-bit weights (bits 16 packing): used for the shared expert. */
 int moe_grouped_gemm_w16a16(const void *a, int a_dtype, const void *packed_w, int64_t E,
                             int64_t K, int64_t N, const int32_t *offsets, int64_t R, int act,

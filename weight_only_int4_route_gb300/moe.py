@@ -63,6 +63,7 @@ _SIGS = {
     "moe_grouped_gemm_workspace_size": (_c_size, [_c_i64, _c_i64, _c_i64, _c_i64, _c_int, _c_int]),
     "moe_grouped_gemm_w4a16": (_c_int, [_vp, _c_int, _vp, _c_i64, _c_i64, _c_i64, _c_int, _vp, _c_i64, _c_int, _vp, _c_int, _vp, _c_size, _vp]),
     "moe_grouped_gemm_w8a16": (_c_int, [_vp, _c_int, _vp, _c_i64, _c_i64, _c_i64, _c_int, _vp, _c_i64, _c_int, _vp, _c_int, _vp, _c_size, _vp]),
+    "moe_grouped_gemm_w4a16_static": (_c_int, [_vp, _c_int, _vp, _c_i64, _c_i64, _c_i64, _c_int, _vp, _c_i64, _c_int, _vp, _c_int, _vp]),
     "moe_grouped_gemm_w16a16": (_c_int, [_vp, _c_int, _vp, _c_i64, _c_i64, _c_i64, _vp, _c_i64, _c_int, _vp, _c_int, _vp, _c_size, _vp]),
     "moe_unpermute_combine": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _c_int, _c_i64, _c_i64, _c_int, _vp, _c_int, _vp]),
     "moe_shared_expert_workspace_size": (_c_size, [_c_i64, _c_i64, _c_i64]),
@@ -199,6 +200,17 @@ def grouped_gemm(a: torch.Tensor, packed: torch.Tensor, bits: int, E: int, K: in
     else:
         st = lib().moe_grouped_gemm_w16a16(*args, *tail)
     _check(st, f"moe_grouped_gemm (bits {bits})")
+    return out
+
+
+def grouped_gemm_static(a: torch.Tensor, packed: torch.Tensor, E: int, K: int, N: int, group: int,
+                        offsets: torch.Tensor, act: str, out_dtype: torch.dtype) -> torch.Tensor:
+    """INT4 grouped GEMM whose scratch lives in the library (no workspace argument)."""
+    R = a.shape[0]
+    out = torch.empty((R, N // 2 if act == "swiglu" else N), dtype=out_dtype, device=a.device)
+    _check(lib().moe_grouped_gemm_w4a16_static(_ptr(a), _dt(a), _ptr(packed), E, K, N, group, _ptr(offsets), R,
+                                               ACT[act], _ptr(out), _TORCH2MOE[out_dtype], _stream(a.device)),
+           "moe_grouped_gemm_w4a16_static")
     return out
 
 
