@@ -121,10 +121,14 @@ int moe_dequant(const void *packed, int w_dtype, int64_t E, int64_t K, int64_t N
  *                  renormalize != 0 the k gates of a token are divided by their sum.
  * x: (T, d) x_dtype (F16|BF16).  w_router: (d, E) wr_dtype (F32|F16|BF16; 16-bit must
  * equal x_dtype).  bias: fp32 (E) or NULL.  ids: int32 (T, k).  gate_w: fp32 (T, k).
- * 1 <= k <= E <= 256, d % 8 == 0.  T == 0 is allowed (nothing is enqueued). */
+ * 1 <= k <= E <= 256, d % 8 == 0.  T == 0 is allowed (nothing is enqueued).
+ * workspace: >= moe_route_topk_workspace_size(T, d, E) bytes for 16-bit router weights (fp32
+ * partial logits of the K splits, summed in split order); unused for fp32 router weights. */
+size_t moe_route_topk_workspace_size(int64_t T, int64_t d, int64_t E);
 int moe_route_topk(const void *x, int x_dtype, const void *w_router, int wr_dtype,
                    const float *bias, int64_t T, int64_t d, int64_t E, int k, int renormalize,
-                   int32_t *ids, float *gate_w, moe_stream_t stream);
+                   int32_t *ids, float *gate_w, void *workspace, size_t workspace_bytes,
+                   moe_stream_t stream);
 
 /* ------------------------------------------------------------------------------------
  * Permute.  [FT] workflow: append the row index to the gating tuple, sort by expert id,
@@ -160,7 +164,8 @@ int moe_permute(const int32_t *ids, const void *x, int x_dtype, int64_t T, int64
  * Algorithm 1 up to rounding order); group-128 scales are applied in the mainloop as
  * RN(q * s) in the operand dtype, as Algorithm 1 states. */
 /* Which kernel a grouped GEMM with these arguments (offsets given) runs: 1 = the tcgen05
- * tensor-memory kernel (many rows per expert), 0 = the warp-MMA kernel (decode batches). */
+ * tensor-memory kernel (>= 64 rows per active expert), 2 = the decode weight-stream kernel
+ * (<= 32 rows per active expert), 0 = the warp-MMA tile kernel (in between). */
 int moe_gemm_path(int64_t R, int64_t E, int64_t K, int64_t N, int bits, int group, int act);
 size_t moe_grouped_gemm_workspace_size(int64_t R, int64_t E, int64_t K, int64_t N, int bits,
                                        int act);

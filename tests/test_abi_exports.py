@@ -17,7 +17,7 @@ def L():
 
 def test_every_header_symbol_is_exported(L):
     names = M.header_symbols()
-    assert len(names) >= 19
+    assert len(names) >= 21
     missing = [n for n in names if not hasattr(L, n)]
     assert missing == []
     assert set(names) == set(M._SIGS), "binding and header disagree"
@@ -51,11 +51,11 @@ def test_invalid_arguments_are_rejected_on_host(L):
     assert L.moe_pack_weights(nul, nul, 0, 1, 256, 64, 5, 0, nul, 0, nul) == -1
     assert b"bits" in L.moe_last_error_string()
     # bad dtype
-    assert L.moe_route_topk(nul, 7, nul, 0, nul, 4, 256, 8, 2, 0, nul, nul, nul) == -1
+    assert L.moe_route_topk(nul, 7, nul, 0, nul, 4, 256, 8, 2, 0, nul, nul, nul, 0, nul) == -1
     # k > E
-    assert L.moe_route_topk(nul, 0, nul, 0, nul, 4, 256, 8, 9, 0, nul, nul, nul) == -1
+    assert L.moe_route_topk(nul, 0, nul, 0, nul, 4, 256, 8, 9, 0, nul, nul, nul, 0, nul) == -1
     # T == 0 is a no-op
-    assert L.moe_route_topk(nul, 0, nul, 0, nul, 0, 256, 8, 2, 0, nul, nul, nul) == 0
+    assert L.moe_route_topk(nul, 0, nul, 0, nul, 0, 256, 8, 2, 0, nul, nul, nul, 0, nul) == 0
     # K not a multiple of 128
     assert L.moe_grouped_gemm_w4a16(nul, 0, nul, 2, 200, 64, 0, nul, 4, 0, nul, 0, nul, 0, nul) == -1
     # unsupported N

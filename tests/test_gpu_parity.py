@@ -223,9 +223,51 @@ def test_gemm_exact_integers(M, bits, group, dtype, counts, N, act):
     assert torch.equal(got.double(), ref), path
 
 
+def _gemv_counts(case):
+    if case == "few_rows":            # one n8 tile per row chunk, two m16 tiles per unit
+        return [1, 0, 3, 2, 5, 0, 7, 8], 1024, 256
+    if case == "two_tiles":           # two n8 tiles per row chunk
+        return [9, 16, 12, 0, 10], 512, 192
+    if case == "many_experts":        # expert table past 128 entries, rows only at high ids
+        c = [0] * 200
+        c[3], c[150], c[199], c[130] = 1, 2, 1, 3
+        return c, 256, 64
+    if case == "split_k":             # two rows, long K: the plan splits K
+        return [2, 1], 4096, 128
+    raise ValueError(case)
+
+
+@pytest.mark.parametrize("bits,group,dtype", [(4, 128, torch.bfloat16), (4, 0, torch.float16),
+                                              (8, 128, torch.float16), (8, 0, torch.bfloat16),
+                                              (16, 0, torch.bfloat16)])
+@pytest.mark.parametrize("case", ["few_rows", "two_tiles", "many_experts", "split_k"])
+@pytest.mark.parametrize("act", ["none", "relu"])
+def test_decode_gemm_exact_integers(M, bits, group, dtype, case, act):
+    """Decode-sized batches (a few rows per expert) on the weight-stream kernel: integer
+    activations and power-of-two scales keep every sum exact, so the result is bit-exact."""
+    counts, K, N = _gemv_counts(case)
+    gen = torch.Generator().manual_seed(len(counts) * 7 + K + N + bits)
+    E, R = len(counts), sum(counts)
+    a = torch.randint(-1, 2, (R, K), generator=gen).to(dtype)
+    if bits == 16:
+        q = torch.randint(-8, 9, (E, K, N), generator=gen).to(dtype)
+        s = None
+        packed = M.pack_weights(q.to(DEV), None, 16, 0)
+    else:
+        q = _codes(bits, (E, K, N), gen)
+        G = 1 if group == 0 else K // 128
+        s = (2.0 ** torch.randint(-7, -4, (E, G, N), generator=gen).double()).to(dtype)
+        packed = M.pack_weights(q.to(DEV), s.to(DEV), bits, group)
+    off = _rows_offsets(counts)
+    assert M.gemm_path(R, E, K, N, bits, group, act) == "gemv"
+    got = M.grouped_gemm(a.to(DEV), packed, bits, E, K, N, group, off.to(DEV), act, torch.float32).cpu()
+    assert M.device_error(DEV) == 0
+    assert torch.equal(got.double(), _oracle_gemm(a, q, s, group, off, act))
+
+
 @pytest.mark.parametrize("name,which", [("tiny", 1), ("tiny", 2), ("encdec_int8", 1), ("encdec_int4", 2),
                                         ("qwen", 1), ("qwen", 2), ("phi", 1)])
-@pytest.mark.parametrize("counts", [[3, 0, 1, 2], [40, 7, 0, 129], [300, 150, 0, 77]])
+@pytest.mark.parametrize("counts", [[3, 0, 1, 2], [12, 9, 0, 16], [40, 7, 0, 129], [300, 150, 0, 77]])
 def test_gemm_config_shapes_vs_oracle(M, name, which, counts):
     """FC1 (with its activation) or FC2 on each config's real (K, N), 4 experts."""
     cfg = synth.CONFIGS[name]

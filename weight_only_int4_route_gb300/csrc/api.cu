@@ -74,7 +74,7 @@ int grouped_gemm(int bits, const void *a, int a_dtype, const void *packed_w, int
                  int out_dtype, void *workspace, size_t workspace_bytes, cudaStream_t st) {
   MOE_TRY(check_gemm_args(bits, a, a_dtype, packed_w, E, K, N, group, offsets, R, act, out, out_dtype));
   if (R == 0) return MOE_OK;
-  const GemmPlan pl = plan_gemm(R, E, K, N, act, false);
+  const GemmPlan pl = plan_gemm(R, E, K, N, bits, act, false);
   const size_t need = gemm_ws_bytes(pl, R, N);
   if (need) {
     MOE_REQUIRE(workspace && aligned16(workspace), "workspace must be non-null and 16-byte aligned");
@@ -107,7 +107,7 @@ int grouped_gemm(int bits, const void *a, int a_dtype, const void *packed_w, int
 struct LayerPlan {
   int64_t T, R;
   GemmPlan fc1, fc2, sh1, sh2;
-  size_t o_ids, o_gate, o_off, o_perm, o_inv, o_pws, o_xp, o_p1, o_h, o_y, o_hs, o_ps1, o_ys, total;
+  size_t o_ids, o_gate, o_off, o_perm, o_inv, o_rws, o_pws, o_xp, o_p1, o_h, o_y, o_hs, o_ps1, o_ys, total;
 };
 
 int check_desc(const moe_layer_desc *d) {
@@ -129,8 +129,8 @@ LayerPlan plan_layer(const moe_layer_desc *d, int64_t T) {
   p.T = T;
   p.R = T * d->k;
   const int64_t F1 = d->act == MOE_ACT_SWIGLU ? 2 * d->F : d->F;
-  p.fc1 = plan_gemm(p.R, d->E, d->d, F1, d->act, false);
-  p.fc2 = plan_gemm(p.R, d->E, d->F, d->d, MOE_ACT_NONE, true);
+  p.fc1 = plan_gemm(p.R, d->E, d->d, F1, d->bits, d->act, false);
+  p.fc2 = plan_gemm(p.R, d->E, d->F, d->d, d->bits, MOE_ACT_NONE, true);
   size_t o = 0;
   auto take = [&](size_t bytes) {
     const size_t at = o;
@@ -142,14 +142,15 @@ LayerPlan plan_layer(const moe_layer_desc *d, int64_t T) {
   p.o_off = take(size_t(d->E + 1) * 4);
   p.o_perm = take(size_t(p.R) * 4);
   p.o_inv = take(size_t(p.R) * 4);
+  p.o_rws = take(moe_route_topk_workspace_size(T, d->d, d->E));
   p.o_pws = take(moe_permute_workspace_size(T, d->E, d->k));
   p.o_xp = take(size_t(p.R) * d->d * 2);
   p.o_p1 = take(p.fc1.partial ? size_t(p.fc1.splits) * p.R * F1 * 4 : 0);
   p.o_h = take(size_t(p.R) * d->F * 2);
   p.o_y = take(size_t(p.fc2.splits) * p.R * d->d * 4);
   if (d->Fs > 0) {
-    p.sh1 = plan_gemm(T, 1, d->d, 2 * d->Fs, MOE_ACT_SWIGLU, false);
-    p.sh2 = plan_gemm(T, 1, d->Fs, d->d, MOE_ACT_NONE, true);
+    p.sh1 = plan_gemm(T, 1, d->d, 2 * d->Fs, 16, MOE_ACT_SWIGLU, false);
+    p.sh2 = plan_gemm(T, 1, d->Fs, d->d, 16, MOE_ACT_NONE, true);
     p.o_hs = take(size_t(T) * d->Fs * 2);
     p.o_ps1 = take(p.sh1.partial ? size_t(p.sh1.splits) * T * 2 * d->Fs * 4 : 0);
     p.o_ys = take(size_t(p.sh2.splits) * T * d->d * 4);
@@ -198,18 +199,18 @@ extern "C" int moe_version(void) { return 1; }
 
 extern "C" int moe_gemm_path(int64_t R, int64_t E, int64_t K, int64_t N, int bits, int group, int act) {
   if (R <= 0 || E < 1 || K < 128 || N < 64) return 0;
-  const GemmPlan pl = plan_gemm(R, E, K, N, act, false);
+  const GemmPlan pl = plan_gemm(R, E, K, N, bits, act, false);
   static const int32_t dummy = 0;
   const GemmArgs g = make_args(bits, nullptr, MOE_F16, nullptr, E, K, N, group, &dummy, R, act, nullptr,
                                MOE_F16, nullptr);
+  if (pl.kind == kKindGemv) return 2;
   return (pl.tc && tc_supported(g)) ? 1 : 0;
 }
 
 extern "C" size_t moe_grouped_gemm_workspace_size(int64_t R, int64_t E, int64_t K, int64_t N, int bits,
                                                   int act) {
-  (void)bits;
   if (R <= 0 || E < 1 || K < 128 || N < 64) return 0;
-  return gemm_ws_bytes(plan_gemm(R, E, K, N, act, false), R, N);
+  return gemm_ws_bytes(plan_gemm(R, E, K, N, bits, act, false), R, N);
 }
 
 extern "C" int moe_grouped_gemm_w4a16(const void *a, int a_dtype, const void *packed_w, int64_t E,
@@ -238,8 +239,8 @@ extern "C" int moe_grouped_gemm_w16a16(const void *a, int a_dtype, const void *p
 
 extern "C" size_t moe_shared_expert_workspace_size(int64_t T, int64_t d, int64_t Fs) {
   if (T <= 0 || d < 128 || Fs < 128) return 0;
-  const GemmPlan p1 = plan_gemm(T, 1, d, 2 * Fs, MOE_ACT_SWIGLU, false);
-  const GemmPlan p2 = plan_gemm(T, 1, Fs, d, MOE_ACT_NONE, true);
+  const GemmPlan p1 = plan_gemm(T, 1, d, 2 * Fs, 16, MOE_ACT_SWIGLU, false);
+  const GemmPlan p2 = plan_gemm(T, 1, Fs, d, 16, MOE_ACT_NONE, true);
   return align256(size_t(T) * Fs * 2) + gemm_ws_bytes(p1, T, 2 * Fs) + gemm_ws_bytes(p2, T, d);
 }
 
@@ -256,8 +257,8 @@ extern "C" int moe_shared_expert(const void *x, int x_dtype, const void *w_gate_
   if (workspace_bytes < need)
     return set_error(MOE_ERR_WORKSPACE, "shared-expert workspace %zu < %zu bytes", workspace_bytes, need);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const GemmPlan p1 = plan_gemm(T, 1, d, 2 * Fs, MOE_ACT_SWIGLU, false);
-  const GemmPlan p2 = plan_gemm(T, 1, Fs, d, MOE_ACT_NONE, true);
+  const GemmPlan p1 = plan_gemm(T, 1, d, 2 * Fs, 16, MOE_ACT_SWIGLU, false);
+  const GemmPlan p2 = plan_gemm(T, 1, Fs, d, 16, MOE_ACT_NONE, true);
   char *ws = static_cast<char *>(workspace);
   void *hs = ws;
   float *pa = reinterpret_cast<float *>(ws + align256(size_t(T) * Fs * 2));
@@ -292,7 +293,7 @@ extern "C" int moe_layer_routing_view(const moe_layer_desc *desc, int64_t T, voi
 extern "C" int moe_layer_launch_count(const moe_layer_desc *desc, int64_t T) {
   if (check_desc(desc) != MOE_OK || T <= 0) return 0;
   const LayerPlan p = plan_layer(desc, T);
-  int n = 1 /*route*/ + 3 /*count, scan, scatter*/ + 1 /*fc1*/ + (p.fc1.partial ? 1 : 0) + 1 /*fc2*/ + 1 /*combine*/;
+  int n = (desc->router_dtype == MOE_F32 ? 1 : 2) /*route*/ + (p.R <= 1024 ? 1 : 3) /*permute*/ + 1 /*fc1*/ + (p.fc1.partial ? 1 : 0) + 1 /*fc2*/ + 1 /*combine*/;
   if (desc->Fs > 0) n += 2 + (p.sh1.partial ? 1 : 0);
   return n;
 }
@@ -341,7 +342,8 @@ extern "C" int moe_layer_forward_profiled(const moe_layer_desc *desc, const moe_
   };
   MOE_TRY(mark(MOE_STAGE_START));
   MOE_TRY(moe_route_topk(x, dt, w->w_router, desc->router_dtype, w->router_bias, T, d, E, k,
-                         desc->renormalize, ids, gate, stream));
+                         desc->renormalize, ids, gate, ws + p.o_rws, moe_route_topk_workspace_size(T, d, E),
+                         stream));
   MOE_TRY(mark(MOE_STAGE_ROUTED));
   MOE_TRY(moe_permute(ids, x, dt, T, d, E, k, offs, perm, inv, xp, ws + p.o_pws,
                       moe_permute_workspace_size(T, E, k), stream));

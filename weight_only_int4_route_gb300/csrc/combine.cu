@@ -31,10 +31,22 @@ __global__ void reduce_act_kernel(const float *__restrict__ part, int splits, in
     const int64_t r = i / Nout;
     const int c = int(i % Nout);
     float v = 0.f;
-    for (int s = 0; s < splits; ++s) v += part[s * slice + r * N + c];
+    const float *pv = part + r * N + c;
+    int s = 0;
+    for (; s + 4 <= splits; s += 4) {
+      const float q0 = pv[s * slice], q1 = pv[(s + 1) * slice], q2 = pv[(s + 2) * slice], q3 = pv[(s + 3) * slice];
+      v += q0; v += q1; v += q2; v += q3;
+    }
+    for (; s < splits; ++s) v += pv[s * slice];
     if (act == MOE_ACT_SWIGLU) {
       float u = 0.f;
-      for (int s = 0; s < splits; ++s) u += part[s * slice + r * N + Nout + c];
+      const float *pu = pv + Nout;
+      s = 0;
+      for (; s + 4 <= splits; s += 4) {
+        const float q0 = pu[s * slice], q1 = pu[(s + 1) * slice], q2 = pu[(s + 2) * slice], q3 = pu[(s + 3) * slice];
+        u += q0; u += q1; u += q2; u += q3;
+      }
+      for (; s < splits; ++s) u += pu[s * slice];
       v = act_silu(v) * u;
     } else {
       v = act_apply(v, act);
@@ -61,12 +73,25 @@ __global__ void combine_kernel(const void *__restrict__ y, int y_dtype, int yspl
       if (p < 0 || p >= R) continue;  // malformed permutation: contributes nothing
       const float gw = gate[tok * k + j];
       float v[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int s = 0; s < ysplits; ++s) {
-        const int64_t base = s * R * d + p * d + c;
-        if (y_dtype == MOE_F32) {
-          const float4 q = *reinterpret_cast<const float4 *>(static_cast<const float *>(y) + base);
+      if (y_dtype == MOE_F32) {
+        const float *yf = static_cast<const float *>(y) + p * d + c;
+        int s = 0;
+        for (; s + 4 <= ysplits; s += 4) {   // four independent loads in flight, summed in split order
+          float4 q[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) q[u] = *reinterpret_cast<const float4 *>(yf + (s + u) * R * d);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            v[0] += q[u].x; v[1] += q[u].y; v[2] += q[u].z; v[3] += q[u].w;
+          }
+        }
+        for (; s < ysplits; ++s) {
+          const float4 q = *reinterpret_cast<const float4 *>(yf + s * R * d);
           v[0] += q.x; v[1] += q.y; v[2] += q.z; v[3] += q.w;
-        } else {
+        }
+      } else {
+        for (int s = 0; s < ysplits; ++s) {
+          const int64_t base = s * R * d + p * d + c;
 #pragma unroll
           for (int q = 0; q < 4; ++q) v[q] += ld_any(y, y_dtype, base + q);
         }
@@ -75,9 +100,27 @@ __global__ void combine_kernel(const void *__restrict__ y, int y_dtype, int yspl
       for (int q = 0; q < 4; ++q) acc[q] += gw * v[q];
     }
     if (sh) {
-      for (int s = 0; s < shsplits; ++s) {
+      if (sh_dtype == MOE_F32) {
+        const float *sf = static_cast<const float *>(sh) + tok * d + c;
+        int s = 0;
+        for (; s + 4 <= shsplits; s += 4) {
+          float4 q[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) acc[q] += ld_any(sh, sh_dtype, s * T * d + tok * d + c + q);
+          for (int u = 0; u < 4; ++u) q[u] = *reinterpret_cast<const float4 *>(sf + (s + u) * T * d);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            acc[0] += q[u].x; acc[1] += q[u].y; acc[2] += q[u].z; acc[3] += q[u].w;
+          }
+        }
+        for (; s < shsplits; ++s) {
+          const float4 q = *reinterpret_cast<const float4 *>(sf + s * T * d);
+          acc[0] += q.x; acc[1] += q.y; acc[2] += q.z; acc[3] += q.w;
+        }
+      } else {
+        for (int s = 0; s < shsplits; ++s) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) acc[q] += ld_any(sh, sh_dtype, s * T * d + tok * d + c + q);
+        }
       }
     }
 #pragma unroll

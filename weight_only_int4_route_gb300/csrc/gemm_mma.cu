@@ -39,6 +39,7 @@ constexpr int kRowBytes = kKC * 2 + 32;
 constexpr int kMaxE = 256;
 constexpr int kEpStride = kNB + 8;  // fp32 epilogue tile row stride
 constexpr int kTcMinRows = 64;      // rows per active expert from which the tcgen05 path is used
+constexpr int kGemvMaxRows = 16;    // rows per active expert up to which the decode stream kernel is used
 
 template <int BITS> struct WT {
   static constexpr int kVec = BITS == 4 ? 1 : (BITS == 8 ? 2 : 4);  // uint4 per lane per chunk
@@ -326,10 +327,12 @@ int64_t est_tiles(int64_t R, int64_t E, int mt) { return std::min<int64_t>(E, R)
 
 }  // namespace
 
-GemmPlan plan_gemm(int64_t R, int64_t E, int64_t K, int64_t N, int act, bool want_partial) {
+GemmPlan plan_gemm(int64_t R, int64_t E, int64_t K, int64_t N, int bits, int act, bool want_partial) {
   GemmPlan pl{};
   const int64_t active = std::max<int64_t>(1, std::min<int64_t>(E, R));
   const int64_t avg = cdiv(std::max<int64_t>(R, 1), active);
+  if (avg <= kGemvMaxRows && gemv_shape_ok(K, N, bits, act)) return plan_gemv(R, E, K, N, bits, act, want_partial);
+  pl.kind = kKindMma;
   pl.mb = avg <= 16 ? 1 : (avg <= 32 ? 2 : 4);
   const int64_t nck = K / kKC;
   const bool swiglu = act == MOE_ACT_SWIGLU;
@@ -345,10 +348,12 @@ GemmPlan plan_gemm(int64_t R, int64_t E, int64_t K, int64_t N, int act, bool wan
   pl.partial = want_partial || pl.splits > 1;
   pl.ncb = int(pl.partial ? N / kNB : ncb_fused);
   pl.tc = pl.splits == 1 && tc_rows;
+  if (pl.tc) pl.kind = kKindTc;
   return pl;
 }
 
 int launch_gemm(const GemmArgs &g, const GemmPlan &pl, cudaStream_t st) {
+  if (pl.kind == kKindGemv) return launch_gemv(g, pl, st);
   if (pl.tc && tc_supported(g) && (!pl.partial || g.act == MOE_ACT_NONE)) {
     GemmArgs t = g;
     if (pl.partial) {  // single split: the fp32 "partial" slice is the output itself

@@ -150,20 +150,6 @@ __device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t (&v)[16])
 }
 __device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
 
-__device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-      "%15}, [%16];\n"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr)
-      : "memory");
-  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
 __device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];
   asm volatile(
@@ -201,12 +187,6 @@ template <typename T> __device__ __forceinline__ float ldscale(const uint16_t *s
   const uint16_t b = s[i];
   if constexpr (std::is_same<T, __half>::value) return __half2float(__ushort_as_half(b));
   else return __bfloat162float(__ushort_as_bfloat16(b));
-}
-
-__device__ __forceinline__ void store_val(void *out, int dt, int64_t i, float v) {
-  if (dt == MOE_F32) static_cast<float *>(out)[i] = v;
-  else if (dt == MOE_F16) static_cast<__half *>(out)[i] = __float2half_rn(v);
-  else static_cast<__nv_bfloat16 *>(out)[i] = __float2bfloat16_rn(v);
 }
 
 struct Tile {

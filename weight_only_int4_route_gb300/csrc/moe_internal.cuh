@@ -42,8 +42,14 @@ inline size_t packed_code_bytes(int64_t E, int64_t K, int64_t N, int bits) {
 }
 inline int64_t scale_groups(int64_t K, int group) { return group == 0 ? 1 : K / group; }
 
-// Split-K / tiling plan of the mma.sync grouped GEMM (shared by size queries and launches).
+// Which grouped-GEMM kernel runs and how it is split (shared by size queries and launches).
+enum : int { kKindMma = 0, kKindTc = 1, kKindGemv = 2 };
 struct GemmPlan {
+  int kind;    // kKindMma (warp MMA, mid-size batches), kKindTc (tcgen05), kKindGemv (decode stream)
+  int nt;      // decode kernel: n8 tiles of routed rows per unit
+  int ch;      // decode kernel: 128-wide chunks per K split
+  int ng;      // decode kernel: channel groups of mt m16 tiles
+  int mt;      // decode kernel: m16 tiles (16 channels each) per unit
   int mb;      // m16 tiles per CTA tile (rows per tile = 16 * mb)
   int splits;  // split-K factor
   int ks;      // K per split (multiple of 128)
@@ -51,7 +57,9 @@ struct GemmPlan {
   bool partial;  // fp32 partial slices instead of the fused epilogue
   bool tc;       // rows per active expert large enough for the tcgen05 path
 };
-GemmPlan plan_gemm(int64_t R, int64_t E, int64_t K, int64_t N, int act, bool want_partial);
+GemmPlan plan_gemm(int64_t R, int64_t E, int64_t K, int64_t N, int bits, int act, bool want_partial);
+bool gemv_shape_ok(int64_t K, int64_t N, int bits, int act);
+GemmPlan plan_gemv(int64_t R, int64_t E, int64_t K, int64_t N, int bits, int act, bool want_partial);
 
 struct GemmArgs {
   const void *a;
@@ -73,6 +81,7 @@ struct GemmArgs {
 // tcgen05 kernel when the plan and the shapes allow it, else to the warp-MMA kernel.
 int launch_gemm(const GemmArgs &g, const GemmPlan &pl, cudaStream_t st);
 int launch_gemm_mma(const GemmArgs &g, const GemmPlan &pl, cudaStream_t st);
+int launch_gemv(const GemmArgs &g, const GemmPlan &pl, cudaStream_t st);
 bool tc_supported(const GemmArgs &g);
 int launch_gemm_tc(const GemmArgs &g, cudaStream_t st);
 int read_device_error(cudaStream_t st, int *out);
@@ -117,30 +126,37 @@ __device__ __forceinline__ __nv_bfloat162 u32_as_b2(uint32_t v) {
 
 // INT4 word -> four 16-bit pairs (e0,e1) (e2,e3) (e4,e5) (e6,e7) holding q = u - 8.
 // Pair p lives in bits 4p and 16 + 4p (nibble slots p and p + 4 of the interleaved word).
+//
+// The steps are written as single PTX instructions (one lop3 per masked OR, one shr per
+// shift): this conversion is the integer-ALU bound part of a weight stream, and the plain C++
+// form of the same expressions was measured to compile to about four more integer instructions
+// per word.
 __device__ __forceinline__ void i2f_int4(uint32_t w, uint32_t (&h)[4], __half) {
-  const uint32_t magic = 0x64006400u;
-  const uint32_t w8 = w >> 8;
-  const uint32_t t0 = (w & 0x000F000Fu) | magic;   // 1024 + u
-  const uint32_t t1 = (w & 0x00F000F0u) | magic;   // 1024 + 16 u   (upper nibble kept in place)
-  const uint32_t t2 = (w8 & 0x000F000Fu) | magic;
-  const uint32_t t3 = (w8 & 0x00F000F0u) | magic;
-  const __half2 bias = __half2half2(__ushort_as_half(0x6408));      // 1032 = 1024 + 8
-  const __half2 sixteenth = __half2half2(__ushort_as_half(0x2C00));  // 1/16
-  const __half2 bias16 = __half2half2(__ushort_as_half(0xD480));     // -72 = -(64 + 8)
-  h[0] = h2_as_u32(__hsub2(u32_as_h2(t0), bias));
-  h[1] = h2_as_u32(__hfma2(u32_as_h2(t1), sixteenth, bias16));
-  h[2] = h2_as_u32(__hsub2(u32_as_h2(t2), bias));
-  h[3] = h2_as_u32(__hfma2(u32_as_h2(t3), sixteenth, bias16));
+  uint32_t w8, t[4];
+  asm("shr.b32 %0, %1, 8;\n" : "=r"(w8) : "r"(w));
+  asm("lop3.b32 %0, %1, 0x000F000F, 0x64006400, 0xEA;\n" : "=r"(t[0]) : "r"(w));    // 1024 + u
+  asm("lop3.b32 %0, %1, 0x00F000F0, 0x64006400, 0xEA;\n" : "=r"(t[1]) : "r"(w));    // 1024 + 16 u
+  asm("lop3.b32 %0, %1, 0x000F000F, 0x64006400, 0xEA;\n" : "=r"(t[2]) : "r"(w8));
+  asm("lop3.b32 %0, %1, 0x00F000F0, 0x64006400, 0xEA;\n" : "=r"(t[3]) : "r"(w8));
+  // lower nibble: (1024 + u) - 1032; upper nibble kept in place: (1024 + 16 u) / 16 - 72
+  const uint32_t bias = 0x64086408u, sixteenth = 0x2C002C00u, bias16 = 0xD480D480u;   // 1032, 1/16, -72
+  asm("sub.f16x2 %0, %1, %2;\n" : "=r"(h[0]) : "r"(t[0]), "r"(bias));
+  asm("fma.rn.f16x2 %0, %1, %2, %3;\n" : "=r"(h[1]) : "r"(t[1]), "r"(sixteenth), "r"(bias16));
+  asm("sub.f16x2 %0, %1, %2;\n" : "=r"(h[2]) : "r"(t[2]), "r"(bias));
+  asm("fma.rn.f16x2 %0, %1, %2, %3;\n" : "=r"(h[3]) : "r"(t[3]), "r"(sixteenth), "r"(bias16));
 }
 
 __device__ __forceinline__ void i2f_int4(uint32_t w, uint32_t (&h)[4], __nv_bfloat16) {
-  const uint32_t magic = 0x43004300u;                                    // 128.0 in bf16
-  const __nv_bfloat162 bias = __bfloat162bfloat162(__ushort_as_bfloat16(0x4308));  // 136 = 128 + 8
+  uint32_t t[4];
+  asm("lop3.b32 %0, %1, 0x000F000F, 0x43004300, 0xEA;\n" : "=r"(t[0]) : "r"(w));    // 128 + u
+  asm("{\n .reg .b32 s;\n shr.b32 s, %1, 4;\n lop3.b32 %0, s, 0x000F000F, 0x43004300, 0xEA;\n}\n"
+      : "=r"(t[1]) : "r"(w));
+  asm("{\n .reg .b32 s;\n shr.b32 s, %1, 8;\n lop3.b32 %0, s, 0x000F000F, 0x43004300, 0xEA;\n}\n"
+      : "=r"(t[2]) : "r"(w));
+  asm("{\n .reg .b32 s;\n shr.b32 s, %1, 12;\n lop3.b32 %0, s, 0x000F000F, 0x43004300, 0xEA;\n}\n"
+      : "=r"(t[3]) : "r"(w));
 #pragma unroll
-  for (int p = 0; p < 4; ++p) {
-    const uint32_t t = ((w >> (4 * p)) & 0x000F000Fu) | magic;           // 128 + u
-    h[p] = h2_as_u32(__hsub2(u32_as_b2(t), bias));
-  }
+  for (int p = 0; p < 4; ++p) asm("sub.bf16x2 %0, %1, %2;\n" : "=r"(h[p]) : "r"(t[p]), "r"(0x43084308u));   // - 136
 }
 
 // INT8 word (byte b = element b, u = q + 128) -> two pairs (e0,e1) (e2,e3).

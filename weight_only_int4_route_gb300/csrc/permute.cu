@@ -99,6 +99,68 @@ __global__ void __launch_bounds__(kTile) scatter_kernel(const int32_t *__restric
   }
 }
 
+
+// Whole permute in one CTA for small batches (R <= 1024 rows, decode steps): per-warp counts,
+// prefix over warps and experts, stable ranks from warp matches, then the row gather; one
+// launch instead of three.
+constexpr int kSmall = 1024;
+
+template <int VEC_BYTES>
+__global__ void __launch_bounds__(kSmall) permute_small_kernel(const int32_t *__restrict__ ids,
+                                                               const uint8_t *__restrict__ x, int R, int E, int k,
+                                                               int64_t row_bytes, int32_t *__restrict__ offsets,
+                                                               int32_t *__restrict__ perm,
+                                                               int32_t *__restrict__ inv_perm,
+                                                               uint8_t *__restrict__ xp) {
+  __shared__ int wcount[kSmall / 32][kMaxE];
+  __shared__ int s_off[kMaxE];
+  __shared__ int dest[kSmall];
+  __shared__ int scratch[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < (kSmall / 32) * E; i += kSmall) wcount[i / E][i % E] = 0;
+  __syncthreads();
+  int e = tid < R ? ids[tid] : -1;
+  if (e >= E) e = -1;
+  const unsigned same = __match_any_sync(0xffffffffu, e);
+  const int rank_in_warp = __popc(same & ((1u << lane) - 1u));
+  if (e >= 0 && rank_in_warp == 0) wcount[warp][e] = __popc(same);
+  __syncthreads();
+  int total = 0;
+  if (tid < E)
+    for (int w = 0; w < kSmall / 32; ++w) {
+      const int c = wcount[w][tid];
+      wcount[w][tid] = total;
+      total += c;
+    }
+  int start = 0;
+  const int all = block_exclusive_scan(tid < E ? total : 0, &start, scratch);
+  if (tid < E) {
+    s_off[tid] = start;
+    offsets[tid] = start;
+  }
+  if (tid == 0) offsets[E] = all;
+  __syncthreads();
+  dest[tid] = -1;
+  if (e >= 0) {
+    const int p = s_off[e] + wcount[warp][e] + rank_in_warp;
+    perm[p] = tid;
+    inv_perm[tid] = p;
+    dest[tid] = p;
+  }
+  __syncthreads();
+  for (int r = warp; r < R; r += kSmall / 32) {
+    if (dest[r] < 0) continue;
+    const uint8_t *src = x + int64_t(r / k) * row_bytes;
+    uint8_t *dst = xp + int64_t(dest[r]) * row_bytes;
+    for (int64_t c = int64_t(lane) * VEC_BYTES; c < row_bytes; c += 32 * VEC_BYTES) {
+      if constexpr (VEC_BYTES == 16)
+        *reinterpret_cast<uint4 *>(dst + c) = *reinterpret_cast<const uint4 *>(src + c);
+      else
+        *reinterpret_cast<uint2 *>(dst + c) = *reinterpret_cast<const uint2 *>(src + c);
+    }
+  }
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -131,13 +193,22 @@ extern "C" int moe_permute(const int32_t *ids, const void *x, int x_dtype, int64
   MOE_REQUIRE(workspace && aligned16(workspace), "workspace must be non-null and 16-byte aligned");
   if (workspace_bytes < need)
     return set_error(MOE_ERR_WORKSPACE, "permute workspace %zu < %zu bytes", workspace_bytes, need);
+  const int64_t row_bytes = d * 2;
+  if (R <= kSmall) {
+    if (row_bytes % 16 == 0)
+      permute_small_kernel<16><<<1, kSmall, 0, st>>>(ids, static_cast<const uint8_t *>(x), int(R), int(E), k, row_bytes,
+                                                     offsets, perm, inv_perm, static_cast<uint8_t *>(xp));
+    else
+      permute_small_kernel<8><<<1, kSmall, 0, st>>>(ids, static_cast<const uint8_t *>(x), int(R), int(E), k, row_bytes,
+                                                    offsets, perm, inv_perm, static_cast<uint8_t *>(xp));
+    return check_launch("permute_small");
+  }
   const int ntiles = int(cdiv(R, kTile));
   int32_t *tile_counts = static_cast<int32_t *>(workspace);
   int32_t *tile_base = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) +
                                                    align256(size_t(ntiles) * size_t(E) * 4));
   count_kernel<<<ntiles, kTile, 0, st>>>(ids, R, int(E), tile_counts);
   scan_kernel<<<1, kMaxE, 0, st>>>(tile_counts, ntiles, int(E), tile_base, offsets);
-  const int64_t row_bytes = d * 2;
   if (row_bytes % 16 == 0)
     scatter_kernel<16><<<ntiles, kTile, 0, st>>>(ids, tile_base, static_cast<const uint8_t *>(x), R,
                                                  int(E), k, row_bytes, perm, inv_perm, static_cast<uint8_t *>(xp));

@@ -5,9 +5,11 @@
 // experts are activated; background on GPTQ INT4: the router stays in 16-bit.
 // "Who Says Elephants Can't Run", section 3 model table: top-1 (Switch) gating.
 //
-// One CTA handles 16 tokens.  16-bit router weights use the warp tensor-core MMA with fp32
-// accumulation (a 16 x E x d product per CTA); fp32 router weights use fp32 FMAs.  The top-k
-// and softmax run one warp per token over the E logits kept in shared memory.
+// 16-bit router weights use the warp tensor-core MMA with fp32 accumulation, split over K so
+// that a decode step (a few tokens) spreads the d x E weight read over many CTAs; partial
+// logits are summed in split order by the top-k kernel (deterministic).  fp32 router weights
+// (small routers) use fp32 FMAs in one kernel.  The top-k and softmax run one warp per token
+// over the E logits kept in shared memory.
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -80,89 +82,6 @@ __device__ void topk_softmax_warp(const float *logits, int E, int k, int renorm,
   }
 }
 
-// 16-bit router weights: tensor-core logits.
-template <typename T>
-__global__ void __launch_bounds__(kThreads) route_mma_kernel(const T *__restrict__ x,
-                                                              const T *__restrict__ wr,
-                                                              const float *__restrict__ bias,
-                                                              int T_, int d, int E, int k,
-                                                              int renorm, int32_t *__restrict__ ids,
-                                                              float *__restrict__ gates) {
-  // The logits tile reuses the weight-chunk storage once the reduction is finished.
-  constexpr int kWsBytes = kMaxE * (kKC + 8) * 2;
-  static_assert(kWsBytes >= kTok * (kMaxE + 1) * 4, "logit tile must fit the weight chunk");
-  __shared__ __align__(16) uint16_t xs[kTok][kKC + 8];
-  __shared__ __align__(16) unsigned char raw[kWsBytes];
-  auto ws = reinterpret_cast<uint16_t(*)[kKC + 8]>(raw);  // transposed chunk: ws[e][kk]
-  auto lg = reinterpret_cast<float(*)[kMaxE + 1]>(raw);
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int g = lane >> 2, t = lane & 3;
-  const int tok0 = blockIdx.x * kTok;
-  const int Ep = (E + 7) & ~7;
-  const int ntiles = Ep / 8;
-  float acc[kMaxE / 8 / 4][4];
-#pragma unroll
-  for (int i = 0; i < kMaxE / 32; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-  const uint16_t *xg = reinterpret_cast<const uint16_t *>(x);
-  const uint16_t *wg = reinterpret_cast<const uint16_t *>(wr);
-  for (int k0 = 0; k0 < d; k0 += kKC) {
-    const int kc = min(kKC, d - k0);
-    for (int i = tid; i < kTok * (kKC / 8); i += kThreads) {  // 16-byte pieces of x
-      const int r = i / (kKC / 8), c8 = (i % (kKC / 8)) * 8;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (tok0 + r < T_ && c8 < kc) v = *reinterpret_cast<const uint4 *>(xg + int64_t(tok0 + r) * d + k0 + c8);
-      *reinterpret_cast<uint4 *>(&xs[r][c8]) = v;
-    }
-    for (int i = tid; i < kKC * Ep; i += kThreads) {
-      const int kk = i / Ep, e = i % Ep;
-      ws[e][kk] = (kk < kc && e < E) ? wg[int64_t(k0 + kk) * E + e] : uint16_t(0);
-    }
-    __syncthreads();
-#pragma unroll
-    for (int ks = 0; ks < kKC / 16; ++ks) {
-      uint32_t a[4];
-      const int c = ks * 16 + 2 * t;
-      a[0] = *reinterpret_cast<const uint32_t *>(&xs[g][c]);
-      a[1] = *reinterpret_cast<const uint32_t *>(&xs[g + 8][c]);
-      a[2] = *reinterpret_cast<const uint32_t *>(&xs[g][c + 8]);
-      a[3] = *reinterpret_cast<const uint32_t *>(&xs[g + 8][c + 8]);
-#pragma unroll
-      for (int i = 0; i < kMaxE / 32; ++i) {
-        const int nt = warp + 4 * i;
-        if (nt < ntiles) {
-          const uint32_t b0 = *reinterpret_cast<const uint32_t *>(&ws[nt * 8 + g][c]);
-          const uint32_t b1 = *reinterpret_cast<const uint32_t *>(&ws[nt * 8 + g][c + 8]);
-          mma16816(acc[i], a, b0, b1, T());
-        }
-      }
-    }
-    __syncthreads();
-  }
-#pragma unroll
-  for (int i = 0; i < kMaxE / 32; ++i) {
-    const int nt = warp + 4 * i;
-    if (nt < ntiles) {
-      const int e0 = nt * 8 + 2 * t;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int e = e0 + h;
-        if (e < E) {
-          const float b = bias ? bias[e] : 0.f;
-          lg[g][e] = acc[i][h] + b;
-          lg[g + 8][e] = acc[i][2 + h] + b;
-        }
-      }
-    }
-  }
-  __syncthreads();
-  for (int r = warp; r < kTok; r += kThreads / 32) {
-    const int tok = tok0 + r;
-    if (tok < T_) topk_softmax_warp(lg[r], E, k, renorm, ids + int64_t(tok) * k, gates + int64_t(tok) * k);
-  }
-}
-
 // fp32 router weights: fp32 FMA logits (small routers).
 template <typename T>
 __global__ void __launch_bounds__(kThreads) route_f32_kernel(const T *__restrict__ x,
@@ -211,14 +130,158 @@ __global__ void __launch_bounds__(kThreads) route_f32_kernel(const T *__restrict
   }
 }
 
+
+// ---- split-K router: partial logits per (K split, token, expert), then a fixed-order reduce ----
+// CTA = 64 tokens (4 warps x m16) x one K range; the router weights are staged row-major with
+// plain coalesced loads and turned into MMA B pairs by 16-bit shared-memory reads.  Decode
+// batches (a handful of tokens) spread the d x E weight read over many CTAs this way.
+constexpr int kPTok = 64;
+constexpr int kPKC = 64;
+constexpr int kPEG = 64;   // experts per pass
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) route_partial_kernel(const T *__restrict__ x, const T *__restrict__ wr,
+                                                                 int T_, int d, int E, int KS,
+                                                                 float *__restrict__ part) {
+  __shared__ __align__(16) uint16_t xs[kPTok][kPKC + 8];
+  __shared__ __align__(16) uint16_t ws[kPKC][kPEG + 8];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const int tok0 = blockIdx.x * kPTok;
+  const int s = blockIdx.y;
+  const int k_begin = s * KS, k_end = min(d, k_begin + KS);
+  const uint16_t *xg = reinterpret_cast<const uint16_t *>(x);
+  const uint16_t *wg = reinterpret_cast<const uint16_t *>(wr);
+  for (int g0 = 0; g0 < E; g0 += kPEG) {
+    const int EG = min(kPEG, E - g0);
+    const int ntiles = (EG + 7) >> 3;
+    float acc[kPEG / 8][4];
+#pragma unroll
+    for (int i = 0; i < kPEG / 8; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+    for (int k0 = k_begin; k0 < k_end; k0 += kPKC) {
+      const int kc = min(kPKC, k_end - k0);
+      for (int i = tid; i < kPTok * (kPKC / 8); i += kThreads) {
+        const int r = i / (kPKC / 8), c8 = (i % (kPKC / 8)) * 8;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (tok0 + r < T_ && c8 < kc) v = *reinterpret_cast<const uint4 *>(xg + int64_t(tok0 + r) * d + k0 + c8);
+        *reinterpret_cast<uint4 *>(&xs[r][c8]) = v;
+      }
+      if ((E & 1) == 0) {
+        // 32-bit words of the (kc x EG) block: every load is issued before any store
+        constexpr int kPer = kPKC * kPEG / 2 / kThreads;
+        uint32_t v[kPer];
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+          const int i = tid + j * kThreads;
+          const int kk = i / (kPEG / 2), ew = i % (kPEG / 2);
+          v[j] = (kk < kc && 2 * ew < EG)
+                     ? *reinterpret_cast<const uint32_t *>(wg + int64_t(k0 + kk) * E + g0 + 2 * ew)
+                     : 0u;
+        }
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+          const int i = tid + j * kThreads;
+          const int kk = i / (kPEG / 2), ew = i % (kPEG / 2);
+          *reinterpret_cast<uint32_t *>(&ws[kk][2 * ew]) = v[j];
+        }
+      } else {
+        for (int i = tid; i < kPKC * kPEG; i += kThreads) {
+          const int kk = i / kPEG, e = i % kPEG;
+          ws[kk][e] = (kk < kc && e < EG) ? wg[int64_t(k0 + kk) * E + g0 + e] : uint16_t(0);
+        }
+      }
+      __syncthreads();
+#pragma unroll
+      for (int ks = 0; ks < kPKC / 16; ++ks) {
+        const int c = ks * 16 + 2 * t;
+        uint32_t a[4];
+        a[0] = *reinterpret_cast<const uint32_t *>(&xs[warp * 16 + g][c]);
+        a[1] = *reinterpret_cast<const uint32_t *>(&xs[warp * 16 + g + 8][c]);
+        a[2] = *reinterpret_cast<const uint32_t *>(&xs[warp * 16 + g][c + 8]);
+        a[3] = *reinterpret_cast<const uint32_t *>(&xs[warp * 16 + g + 8][c + 8]);
+#pragma unroll
+        for (int nt = 0; nt < kPEG / 8; ++nt) {
+          if (nt < ntiles) {
+            const int e = nt * 8 + g;
+            const uint32_t b0 = uint32_t(ws[c][e]) | (uint32_t(ws[c + 1][e]) << 16);
+            const uint32_t b1 = uint32_t(ws[c + 8][e]) | (uint32_t(ws[c + 9][e]) << 16);
+            mma16816(acc[nt], a, b0, b1, T());
+          }
+        }
+      }
+      __syncthreads();
+    }
+#pragma unroll
+    for (int nt = 0; nt < kPEG / 8; ++nt) {
+      if (nt < ntiles) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int e = nt * 8 + 2 * t + h;
+          const int r0 = tok0 + warp * 16 + g;
+          if (e < EG) {
+            if (r0 < T_) part[(int64_t(s) * T_ + r0) * E + g0 + e] = acc[nt][h];
+            if (r0 + 8 < T_) part[(int64_t(s) * T_ + r0 + 8) * E + g0 + e] = acc[nt][2 + h];
+          }
+        }
+      }
+    }
+  }
+}
+
+// One warp per token: logits = sum over K splits in split order (+ bias), then top-k / softmax.
+__global__ void __launch_bounds__(kThreads) route_reduce_topk_kernel(const float *__restrict__ part, int S, int T_,
+                                                                     int E, const float *__restrict__ bias, int k,
+                                                                     int renorm, int32_t *__restrict__ ids,
+                                                                     float *__restrict__ gates) {
+  __shared__ float lg[kThreads / 32][kMaxE];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int tok = blockIdx.x * (kThreads / 32) + warp;
+  if (tok >= T_) return;
+  const int64_t sstride = int64_t(T_) * E;
+  for (int e = lane; e < E; e += 32) {
+    const float *pe = part + int64_t(tok) * E + e;
+    float v = 0.f;
+    int s = 0;
+    for (; s + 8 <= S; s += 8) {   // eight independent loads in flight, summed in split order
+      float q[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) q[u] = pe[(s + u) * sstride];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v += q[u];
+    }
+    for (; s < S; ++s) v += pe[s * sstride];
+    lg[warp][e] = v + (bias ? bias[e] : 0.f);
+  }
+  __syncwarp();
+  topk_softmax_warp(lg[warp], E, k, renorm, ids + int64_t(tok) * k, gates + int64_t(tok) * k);
+}
+
+int route_splits(int64_t T, int64_t d) {
+  const int64_t ntt = cdiv(T, kPTok);
+  const int64_t nkc = cdiv(d, kPKC);
+  int64_t S = cdiv(2 * int64_t(num_sms()), ntt);
+  if (S > nkc) S = nkc;
+  if (S < 1) S = 1;
+  const int64_t ks = cdiv(nkc, S) * kPKC;
+  return int(cdiv(d, ks));
+}
+
 }  // namespace
 }  // namespace moe
 
 using namespace moe;
 
+extern "C" size_t moe_route_topk_workspace_size(int64_t T, int64_t d, int64_t E) {
+  if (T <= 0 || d < 8 || E < 1) return 0;
+  return align256(size_t(route_splits(T, d)) * size_t(T) * size_t(E) * 4);
+}
+
 extern "C" int moe_route_topk(const void *x, int x_dtype, const void *w_router, int wr_dtype,
                               const float *bias, int64_t T, int64_t d, int64_t E, int k,
-                              int renormalize, int32_t *ids, float *gate_w, moe_stream_t stream) {
+                              int renormalize, int32_t *ids, float *gate_w, void *workspace,
+                              size_t workspace_bytes, moe_stream_t stream) {
   MOE_REQUIRE(is16(x_dtype), "x_dtype must be MOE_F16 or MOE_BF16");
   MOE_REQUIRE(wr_dtype == MOE_F32 || wr_dtype == x_dtype, "router weights must be fp32 or the x dtype");
   MOE_REQUIRE(T >= 0 && d >= 8 && d % 8 == 0, "need T >= 0 and d %% 8 == 0 (d=%lld)", (long long)d);
@@ -239,12 +302,24 @@ extern "C" int moe_route_topk(const void *x, int x_dtype, const void *w_router, 
     else
       route_f32_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(static_cast<const __nv_bfloat16 *>(x),
           static_cast<const float *>(w_router), bias, int(T), int(d), int(E), k, renormalize, ids, gate_w);
-  } else if (x_dtype == MOE_F16) {
-    route_mma_kernel<__half><<<grid, kThreads, 0, st>>>(static_cast<const __half *>(x),
-        static_cast<const __half *>(w_router), bias, int(T), int(d), int(E), k, renormalize, ids, gate_w);
   } else {
-    route_mma_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(static_cast<const __nv_bfloat16 *>(x),
-        static_cast<const __nv_bfloat16 *>(w_router), bias, int(T), int(d), int(E), k, renormalize, ids, gate_w);
+    const size_t need = moe_route_topk_workspace_size(T, d, E);
+    MOE_REQUIRE(workspace && aligned16(workspace), "workspace must be non-null and 16-byte aligned");
+    if (workspace_bytes < need)
+      return set_error(MOE_ERR_WORKSPACE, "router workspace %zu < %zu bytes", workspace_bytes, need);
+    const int S = route_splits(T, d);
+    const int KS = int(cdiv(cdiv(d, kPKC), S) * kPKC);
+    float *part = static_cast<float *>(workspace);
+    const dim3 pgrid(unsigned(cdiv(T, kPTok)), unsigned(S));
+    if (x_dtype == MOE_F16)
+      route_partial_kernel<__half><<<pgrid, kThreads, 0, st>>>(static_cast<const __half *>(x),
+          static_cast<const __half *>(w_router), int(T), int(d), int(E), KS, part);
+    else
+      route_partial_kernel<__nv_bfloat16><<<pgrid, kThreads, 0, st>>>(static_cast<const __nv_bfloat16 *>(x),
+          static_cast<const __nv_bfloat16 *>(w_router), int(T), int(d), int(E), KS, part);
+    MOE_TRY(check_launch("route_partial"));
+    route_reduce_topk_kernel<<<unsigned(cdiv(T, kThreads / 32)), kThreads, 0, st>>>(part, S, int(T), int(E), bias, k,
+                                                                                 renormalize, ids, gate_w);
   }
   return check_launch("route_topk");
 }

@@ -56,7 +56,8 @@ _SIGS = {
     "moe_packed_scale_offset": (_c_size, [_c_i64, _c_i64, _c_i64, _c_int]),
     "moe_pack_weights": (_c_int, [_vp, _vp, _c_int, _c_i64, _c_i64, _c_i64, _c_int, _c_int, _vp, _c_size, _vp]),
     "moe_dequant": (_c_int, [_vp, _c_int, _c_i64, _c_i64, _c_i64, _c_int, _c_int, _c_int, _vp, _vp]),
-    "moe_route_topk": (_c_int, [_vp, _c_int, _vp, _c_int, _vp, _c_i64, _c_i64, _c_i64, _c_int, _c_int, _vp, _vp, _vp]),
+    "moe_route_topk_workspace_size": (_c_size, [_c_i64, _c_i64, _c_i64]),
+    "moe_route_topk": (_c_int, [_vp, _c_int, _vp, _c_int, _vp, _c_i64, _c_i64, _c_i64, _c_int, _c_int, _vp, _vp, _vp, _c_size, _vp]),
     "moe_permute_workspace_size": (_c_size, [_c_i64, _c_i64, _c_int]),
     "moe_permute": (_c_int, [_vp, _vp, _c_int, _c_i64, _c_i64, _c_i64, _c_int, _vp, _vp, _vp, _vp, _vp, _c_size, _vp]),
     "moe_gemm_path": (_c_int, [_c_i64, _c_i64, _c_i64, _c_i64, _c_int, _c_int, _c_int]),
@@ -161,8 +162,10 @@ def route_topk(x: torch.Tensor, wr: torch.Tensor, bias: Optional[torch.Tensor], 
     E = wr.shape[1]
     ids = torch.empty((T, k), dtype=torch.int32, device=x.device)
     gate = torch.empty((T, k), dtype=torch.float32, device=x.device)
+    wsb = int(lib().moe_route_topk_workspace_size(T, d, E))
+    ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=x.device)
     _check(lib().moe_route_topk(_ptr(x), _dt(x), _ptr(wr), _dt(wr), _ptr(bias), T, d, E, k, int(renormalize),
-                                _ptr(ids), _ptr(gate), _stream(x.device)), "moe_route_topk")
+                                _ptr(ids), _ptr(gate), _ptr(ws), ws.numel(), _stream(x.device)), "moe_route_topk")
     return ids, gate
 
 
@@ -215,8 +218,8 @@ def grouped_gemm_static(a: torch.Tensor, packed: torch.Tensor, E: int, K: int, N
 
 
 def gemm_path(R, E, K, N, bits, group, act: str) -> str:
-    """'tcgen05' or 'mma': the kernel a grouped GEMM of this shape dispatches to."""
-    return "tcgen05" if lib().moe_gemm_path(R, E, K, N, bits, group, ACT[act]) == 1 else "mma"
+    """'tcgen05', 'gemv' or 'mma': the kernel a grouped GEMM of this shape dispatches to."""
+    return {0: "mma", 1: "tcgen05", 2: "gemv"}[lib().moe_gemm_path(R, E, K, N, bits, group, ACT[act])]
 
 
 def unpermute_combine(yp: torch.Tensor, inv_perm: torch.Tensor, gate: torch.Tensor,
