@@ -292,12 +292,23 @@ def run_ours(args, cfg, T, n_layers, world, rank, local):
     offs = layers[0].routing(T)["offsets"].cpu().tolist()
     counts = [offs[i + 1] - offs[i] for i in range(cfg.E)]
     launches_per_layer = layers[0].launch_count(T)
+    # a kernel that gave up on a bounded wait leaves a code in the device error word: the run's
+    # outputs and times are then not valid, so no number is reported
+    derr = M.device_error(dev)
+    if derr:
+        raise SystemExit(f"bench: device error word {derr} set during the run (a bounded wait expired); "
+                         "no result reported")
+    kinds = {"tcgen05": "gemm_tc_kernel", "gemv": "gemv_kernel", "mma": "gemm_mma_kernel"}
+    F1 = 2 * cfg.F if cfg.act == "swiglu" else cfg.F
+    R = T * cfg.k
+    kernels = {"fc1": kinds[M.gemm_path(R, cfg.E, cfg.d, F1, cfg.bits, cfg.group, cfg.act)],
+               "fc2": kinds[M.gemm_path(R, cfg.E, cfg.F, cfg.d, cfg.bits, cfg.group, "none")]}
 
     ms = max_over_ranks(elapsed_ms / args.steps, dist, dev)
     if e2e is not None:
         e2e["ms"] = max_over_ranks(e2e["ms"], dist, dev)
     return dict(ms=ms, stage_ms=stage_ms, counts=counts, clocks=clk, e2e=e2e, copies=copies,
-                launches=launches_per_layer * n_layers * args.steps, per_layer_bytes=per_layer,
+                launches=launches_per_layer * n_layers * args.steps, per_layer_bytes=per_layer, kernels=kernels,
                 est_touch=est_touch, dist=dist)
 
 
@@ -381,7 +392,7 @@ def main():
         achieved = work["bytes"] / (dom_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "peak_source": f"{peak_src} HBM copy bandwidth"}
-    roof.update({"traffic": None, "kernel": f"grouped GEMM {dom.upper()} (gemm_mma_kernel)",
+    roof.update({"traffic": None, "kernel": f"grouped GEMM {dom.upper()} ({r['kernels'][dom]})",
                  "algorithmic_bytes": work["bytes"], "algorithmic_flops": work["flops"], "ms_per_launch": dom_ms})
     layer_ms = r["ms"] / n_layers
     lw = wm["layer"]

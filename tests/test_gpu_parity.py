@@ -161,9 +161,10 @@ def test_unpermute_of_permute_is_identity(M):
     assert torch.equal(out.cpu(), x)
 
 
-def test_combine_matches_oracle(M):
-    gen = torch.Generator().manual_seed(10)
-    T, k, d = 37, 3, 96
+@pytest.mark.parametrize("T,k,d", [(37, 3, 96), (5, 40, 260), (300, 1, 1024)])
+def test_combine_matches_oracle(M, T, k, d):
+    """Weighted un-permute: d not a multiple of the 128-column group, and k above 32."""
+    gen = torch.Generator().manual_seed(10 + T + k + d)
     y = torch.randn((T * k, d), generator=gen, dtype=torch.float32)
     inv = torch.randperm(T * k, generator=gen).to(torch.int32)
     gate = torch.rand((T, k), generator=gen)
@@ -364,3 +365,24 @@ def test_layer_zero_tokens(M):
     x = torch.empty((0, cfg.d), dtype=cfg.torch_dtype, device=DEV)
     out = layer.forward(x)
     assert out.shape == (0, cfg.d)
+
+
+def test_tcgen05_gemm_repeatable(M):
+    """The tensor-memory GEMM run many times on one prefill shape: no bounded wait may expire
+    and every result is bit-identical (fixed reduction order, no atomics)."""
+    cfg = synth.CONFIGS["encdec_int4"]
+    E, K, N, T = cfg.E, cfg.F, cfg.d, 3840
+    counts = [T // E] * E
+    R = sum(counts)
+    assert M.gemm_path(R, E, K, N, cfg.bits, cfg.group, "none") == "tcgen05"
+    gen = torch.Generator().manual_seed(77)
+    q = _codes(cfg.bits, (E, K, N), gen)
+    s = _scales((E, 1, N), cfg.torch_dtype, gen)
+    packed = M.pack_weights(q.to(DEV), s.to(DEV), cfg.bits, cfg.group)
+    a = torch.randn((R, K), generator=gen).to(cfg.torch_dtype).to(DEV)
+    off = _rows_offsets(counts).to(DEV)
+    first = M.grouped_gemm(a, packed, cfg.bits, E, K, N, cfg.group, off, "none", torch.float32)
+    for _ in range(400):
+        again = M.grouped_gemm(a, packed, cfg.bits, E, K, N, cfg.group, off, "none", torch.float32)
+        assert torch.equal(again, first)
+    assert M.device_error(DEV) == 0

@@ -293,7 +293,7 @@ extern "C" int moe_layer_routing_view(const moe_layer_desc *desc, int64_t T, voi
 extern "C" int moe_layer_launch_count(const moe_layer_desc *desc, int64_t T) {
   if (check_desc(desc) != MOE_OK || T <= 0) return 0;
   const LayerPlan p = plan_layer(desc, T);
-  int n = (desc->router_dtype == MOE_F32 ? 1 : 2) /*route*/ + (p.R <= 1024 ? 1 : 3) /*permute*/ + 1 /*fc1*/ + (p.fc1.partial ? 1 : 0) + 1 /*fc2*/ + 1 /*combine*/;
+  int n = (desc->router_dtype == MOE_F32 ? 1 : 2) /*route*/ + permute_launches(p.R, desc->E) /*permute*/ + 1 /*fc1*/ + (p.fc1.partial ? 1 : 0) + 1 /*fc2*/ + 1 /*combine*/;
   if (desc->Fs > 0) n += 2 + (p.sh1.partial ? 1 : 0);
   return n;
 }

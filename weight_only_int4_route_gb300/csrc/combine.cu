@@ -9,11 +9,6 @@
 namespace moe {
 namespace {
 
-__device__ __forceinline__ float ld_any(const void *p, int dt, int64_t i) {
-  if (dt == MOE_F32) return static_cast<const float *>(p)[i];
-  if (dt == MOE_F16) return __half2float(static_cast<const __half *>(p)[i]);
-  return __bfloat162float(static_cast<const __nv_bfloat16 *>(p)[i]);
-}
 __device__ __forceinline__ void st_any(void *p, int dt, int64_t i, float v) {
   if (dt == MOE_F32) static_cast<float *>(p)[i] = v;
   else if (dt == MOE_F16) static_cast<__half *>(p)[i] = __float2half_rn(v);
@@ -55,76 +50,149 @@ __global__ void reduce_act_kernel(const float *__restrict__ part, int splits, in
   }
 }
 
-// One thread per (token, 4 columns); y has `ysplits` slices of (R, d), sh `shsplits` of (T, d).
-__global__ void combine_kernel(const void *__restrict__ y, int y_dtype, int ysplits,
-                               const int32_t *__restrict__ inv_perm, const float *__restrict__ gate,
-                               const void *__restrict__ sh, int sh_dtype, int shsplits, int64_t T,
-                               int64_t d, int k, void *__restrict__ out, int out_dtype) {
+// Work item = (TPW consecutive tokens, column group of 128 * CPT columns), one per warp; y has
+// `ysplits` slices of (R, d), sh `shsplits` of (T, d).  Lane l reads one (token, entry) row
+// position and gate (32 at a time) and broadcasts them; lane l covers columns 4l .. 4l+3 of each
+// 128 of the group, so a position read feeds CPT independent row loads.  Many tokens: TPW = 2,
+// CPT = 4 (bytes in flight per position read); a few tokens: 1 x 1 (parallelism across columns).
+// Every sum runs in entry order, split slices in split order.
+constexpr int kCombineWarps = 8;
+
+__device__ __forceinline__ float4 ld4(const void *p, int dt, int64_t i) {
+  if (dt == MOE_F32) return *reinterpret_cast<const float4 *>(static_cast<const float *>(p) + i);
+  const uint2 v = *reinterpret_cast<const uint2 *>(static_cast<const char *>(p) + i * 2);
+  if (dt == MOE_F16) {
+    const float2 a = __half22float2(u32_as_h2(v.x)), b = __half22float2(u32_as_h2(v.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+  }
+  const float2 a = __bfloat1622float2(u32_as_b2(v.x)), b = __bfloat1622float2(u32_as_b2(v.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+__device__ __forceinline__ void add4(float (&a)[4], const float4 &q) {
+  a[0] += q.x; a[1] += q.y; a[2] += q.z; a[3] += q.w;
+}
+// acc += sum over s < splits of src[(s * rows + row) * d + c], in split order
+__device__ __forceinline__ void split_sum(const void *src, int dt, int splits, int64_t rows, int64_t row, int64_t d,
+                                          int64_t c, float (&acc)[4]) {
+  int s = 0;
+  for (; s + 8 <= splits; s += 8) {
+    float4 q[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) q[u] = ld4(src, dt, ((s + u) * rows + row) * d + c);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) add4(acc, q[u]);
+  }
+  for (; s < splits; ++s) add4(acc, ld4(src, dt, (s * rows + row) * d + c));
+}
+
+template <int CPT, int TPW>
+__global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(
+    const void *__restrict__ y, int y_dtype, int ysplits, const int32_t *__restrict__ inv_perm,
+    const float *__restrict__ gate, const void *__restrict__ sh, int sh_dtype, int shsplits, int64_t T,
+    int64_t d, int k, void *__restrict__ out, int out_dtype) {
+  const int lane = threadIdx.x & 31;
   const int64_t R = T * k;
-  const int64_t d4 = d / 4;
-  const int64_t total = T * d4;
-  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
-       i += int64_t(gridDim.x) * blockDim.x) {
-    const int64_t tok = i / d4;
-    const int64_t c = (i % d4) * 4;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int j = 0; j < k; ++j) {
-      const int64_t p = inv_perm[tok * k + j];
-      if (p < 0 || p >= R) continue;  // malformed permutation: contributes nothing
-      const float gw = gate[tok * k + j];
-      float v[4] = {0.f, 0.f, 0.f, 0.f};
-      if (y_dtype == MOE_F32) {
-        const float *yf = static_cast<const float *>(y) + p * d + c;
-        int s = 0;
-        for (; s + 4 <= ysplits; s += 4) {   // four independent loads in flight, summed in split order
-          float4 q[4];
+  const int64_t ngroups = (d + 128 * CPT - 1) / (128 * CPT);
+  const int64_t nblk = (T + TPW - 1) / TPW;
+  for (int64_t task = int64_t(blockIdx.x) * kCombineWarps + (threadIdx.x >> 5); task < nblk * ngroups;
+       task += int64_t(gridDim.x) * kCombineWarps) {   // warp-uniform
+    const int64_t tok0 = (task / ngroups) * TPW;
+    const int64_t cbase = (task % ngroups) * 128 * CPT + int64_t(lane) * 4;
+    float acc[TPW][CPT][4];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) q[u] = *reinterpret_cast<const float4 *>(yf + (s + u) * R * d);
+    for (int i = 0; i < TPW; ++i)
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            v[0] += q[u].x; v[1] += q[u].y; v[2] += q[u].z; v[3] += q[u].w;
-          }
-        }
-        for (; s < ysplits; ++s) {
-          const float4 q = *reinterpret_cast<const float4 *>(yf + s * R * d);
-          v[0] += q.x; v[1] += q.y; v[2] += q.z; v[3] += q.w;
-        }
-      } else {
-        for (int s = 0; s < ysplits; ++s) {
-          const int64_t base = s * R * d + p * d + c;
+      for (int u = 0; u < CPT; ++u)
 #pragma unroll
-          for (int q = 0; q < 4; ++q) v[q] += ld_any(y, y_dtype, base + q);
+        for (int q = 0; q < 4; ++q) acc[i][u][q] = 0.f;
+    // entries of the TPW tokens, flattened (token i, entry j) -> i * k + j, 32 per round
+    const int nent = TPW * k;
+    for (int jb = 0; jb < nent; jb += 32) {
+      int pl = -1;
+      float gl = 0.f;
+      {
+        const int l = jb + lane;
+        const int64_t tok = tok0 + l / k;
+        if (l < nent && tok < T) {
+          pl = inv_perm[tok * k + l % k];
+          gl = gate[tok * k + l % k];
+          if (pl < 0 || pl >= R) pl = -1;   // malformed permutation: contributes nothing
         }
       }
+      const int nj = nent - jb < 32 ? nent - jb : 32;
+      if (ysplits == 1 && TPW * k <= 32) {   // one slice: every row load of the round in flight together
+        float4 q[TPW][CPT];
+        float gw[TPW];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) acc[q] += gw * v[q];
-    }
-    if (sh) {
-      if (sh_dtype == MOE_F32) {
-        const float *sf = static_cast<const float *>(sh) + tok * d + c;
-        int s = 0;
-        for (; s + 4 <= shsplits; s += 4) {
-          float4 q[4];
+        for (int i = 0; i < TPW; ++i) gw[i] = 0.f;
+        for (int j = 0; j < k; ++j) {
 #pragma unroll
-          for (int u = 0; u < 4; ++u) q[u] = *reinterpret_cast<const float4 *>(sf + (s + u) * T * d);
+          for (int i = 0; i < TPW; ++i) {
+            const int p = __shfl_sync(0xffffffffu, pl, i * k + j);
+            gw[i] = __shfl_sync(0xffffffffu, gl, i * k + j);
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            acc[0] += q[u].x; acc[1] += q[u].y; acc[2] += q[u].z; acc[3] += q[u].w;
+            for (int u = 0; u < CPT; ++u) {
+              const int64_t c = cbase + u * 128;
+              q[i][u] = (p >= 0 && c < d) ? ld4(y, y_dtype, int64_t(p) * d + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
           }
-        }
-        for (; s < shsplits; ++s) {
-          const float4 q = *reinterpret_cast<const float4 *>(sf + s * T * d);
-          acc[0] += q.x; acc[1] += q.y; acc[2] += q.z; acc[3] += q.w;
+#pragma unroll
+          for (int i = 0; i < TPW; ++i)
+#pragma unroll
+            for (int u = 0; u < CPT; ++u) {
+              acc[i][u][0] += gw[i] * q[i][u].x;
+              acc[i][u][1] += gw[i] * q[i][u].y;
+              acc[i][u][2] += gw[i] * q[i][u].z;
+              acc[i][u][3] += gw[i] * q[i][u].w;
+            }
         }
       } else {
-        for (int s = 0; s < shsplits; ++s) {
+        for (int jj = 0; jj < nj; ++jj) {
+          const int p = __shfl_sync(0xffffffffu, pl, jj);
+          const float gw = __shfl_sync(0xffffffffu, gl, jj);
+          if (p < 0) continue;
+          const int i = (jb + jj) / k;   // token of this entry within the block
 #pragma unroll
-          for (int q = 0; q < 4; ++q) acc[q] += ld_any(sh, sh_dtype, s * T * d + tok * d + c + q);
+          for (int ii = 0; ii < TPW; ++ii) {
+            if (ii != i) continue;
+#pragma unroll
+            for (int u = 0; u < CPT; ++u) {
+              const int64_t c = cbase + u * 128;
+              if (c >= d) continue;
+              float v[4] = {0.f, 0.f, 0.f, 0.f};
+              split_sum(y, y_dtype, ysplits, R, p, d, c, v);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) acc[ii][u][q] += gw * v[q];
+            }
+          }
         }
       }
     }
 #pragma unroll
-    for (int q = 0; q < 4; ++q) st_any(out, out_dtype, tok * d + c + q, acc[q]);
+    for (int i = 0; i < TPW; ++i) {
+      const int64_t tok = tok0 + i;
+      if (tok >= T) continue;
+#pragma unroll
+      for (int u = 0; u < CPT; ++u) {
+        const int64_t c = cbase + u * 128;
+        if (c >= d) continue;
+        if (sh) split_sum(sh, sh_dtype, shsplits, T, tok, d, c, acc[i][u]);
+        if (out_dtype == MOE_F32) {
+          *reinterpret_cast<float4 *>(static_cast<float *>(out) + tok * d + c) =
+              make_float4(acc[i][u][0], acc[i][u][1], acc[i][u][2], acc[i][u][3]);
+        } else {   // four 16-bit values in one 8-byte store
+          uint2 v;
+          if (out_dtype == MOE_F16) {
+            v.x = h2_as_u32(__floats2half2_rn(acc[i][u][0], acc[i][u][1]));
+            v.y = h2_as_u32(__floats2half2_rn(acc[i][u][2], acc[i][u][3]));
+          } else {
+            v.x = h2_as_u32(__floats2bfloat162_rn(acc[i][u][0], acc[i][u][1]));
+            v.y = h2_as_u32(__floats2bfloat162_rn(acc[i][u][2], acc[i][u][3]));
+          }
+          *reinterpret_cast<uint2 *>(static_cast<char *>(out) + (tok * d + c) * 2) = v;
+        }
+      }
+    }
   }
 }
 
@@ -148,8 +216,20 @@ int launch_combine(const void *y, int y_dtype, int ysplits, const int32_t *inv_p
                    const float *gate, const void *sh, int sh_dtype, int shsplits, int64_t T,
                    int64_t d, int k, void *out, int out_dtype, cudaStream_t st) {
   if (T == 0) return MOE_OK;
-  combine_kernel<<<grid_1d(T * (d / 4), 256), 256, 0, st>>>(y, y_dtype, ysplits, inv_perm, gate, sh,
-                                                           sh_dtype, shsplits, T, d, k, out, out_dtype);
+  // two tokens x four 128-column strides per warp when that still leaves 16 work items per SM,
+  // else one token x one stride (parallelism across columns for a few tokens)
+  const int64_t g1 = T * cdiv(d, 128);
+  const bool wide = g1 / 8 >= int64_t(num_sms()) * 16;
+  const int64_t tasks = wide ? cdiv(T, 2) * cdiv(d, 512) : g1;
+  const int64_t want = cdiv(tasks, kCombineWarps);
+  const int64_t cap = int64_t(num_sms()) * 8;
+  const unsigned grid = unsigned(want < cap ? want : cap);
+  if (wide)
+    combine_kernel<4, 2><<<grid, kCombineWarps * 32, 0, st>>>(y, y_dtype, ysplits, inv_perm, gate, sh, sh_dtype,
+                                                              shsplits, T, d, k, out, out_dtype);
+  else
+    combine_kernel<1, 1><<<grid, kCombineWarps * 32, 0, st>>>(y, y_dtype, ysplits, inv_perm, gate, sh, sh_dtype,
+                                                              shsplits, T, d, k, out, out_dtype);
   return check_launch("combine");
 }
 

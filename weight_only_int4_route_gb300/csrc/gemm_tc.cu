@@ -19,8 +19,8 @@
 //                columns; scale / activation, global stores;
 //   warp 8       producer: TMA of the packed weight block and the activation block;
 //   warp 9       MMA issuer (one thread);
-//   warps 10-21  dequant, three groups of four warps; group g converts the K blocks with
-//                index = g (mod 3).  Warp w owns TMEM lanes 32*(w%4).. (one output channel
+//   warps 10-17  dequant, two groups of four warps; group g converts the K blocks with
+//                index = g (mod 2), so each pipeline stage always belongs to the same group.  Warp w owns TMEM lanes 32*(w%4).. (one output channel
 //                per lane); it reads that channel's packed words from shared memory,
 //                converts them with the magic-number I2F (and the group-128 scale) and
 //                stores the 16-bit pairs into the A stage.
@@ -48,13 +48,19 @@ __device__ int g_moe_device_error = 0;
 namespace {
 
 constexpr int kEpiWarps = 8;        // epilogue warps (two per TMEM lane quarter)
-constexpr int kDqGroups = 3;        // dequant warp groups (each: 4 warps covering 128 lanes)
+constexpr int kDqGroups = 2;        // dequant warp groups (each: 4 warps covering 128 lanes)
 constexpr int kProdWarp = kEpiWarps, kMmaWarp = kEpiWarps + 1, kDqWarp0 = kEpiWarps + 2;
 constexpr int kThreads = (kDqWarp0 + 4 * kDqGroups) * 32;
 constexpr int kBM = 128;          // output channels per tile (MMA M)
 constexpr int kBN = 128;          // rows per tile (MMA N upper bound)
 constexpr int kBK = 128;          // K per pipeline stage
 constexpr int kStages = 4;        // pipeline stages (shared memory and TMEM A)
+// Every fill of a stage must go to the same dequant group.  A group waits on full[s] by phase
+// parity, which cannot tell "one phase ahead" from "complete": with groups taking K blocks
+// round-robin over a stage count they do not divide, the group of fill it + kStages could reach
+// full[s] while fill it (another group's) was still in flight -- TMA completions of different
+// stages are not ordered -- and pass the wait at once.
+static_assert(kStages % kDqGroups == 0, "each stage must belong to one dequant group");
 constexpr int kMaxE = 256;
 constexpr int kBHalf = kBN * 64 * 2;         // one 64-wide swizzle atom column block: 16 KB
 constexpr int kBBytes = 2 * kBHalf;          // activation stage: 32 KB

@@ -85,6 +85,8 @@ int launch_gemv(const GemmArgs &g, const GemmPlan &pl, cudaStream_t st);
 bool tc_supported(const GemmArgs &g);
 int launch_gemm_tc(const GemmArgs &g, cudaStream_t st);
 int read_device_error(cudaStream_t st, int *out);
+// Kernel launches of one moe_permute call for R rows over E experts.
+int permute_launches(int64_t R, int64_t E);
 // out[r, c] = act(sum_s part[s, r, c]) (SWIGLU pairs column c with c + N/2).
 int launch_reduce_act(const float *part, int splits, int64_t R, int N, int act, void *out,
                       int out_dtype, cudaStream_t st);

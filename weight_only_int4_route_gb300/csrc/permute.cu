@@ -6,10 +6,15 @@
 // is permuted by the result.  The page uses a library radix sort; with at most 256 keys a
 // three-pass counting sort gives the same (stable) order:
 //   1. per 256-row tile, count rows per expert;
-//   2. one CTA turns the tile counts into expert offsets and per-(tile, expert) bases;
+//   2. the tile counts become expert offsets and per-(tile, expert) bases (one CTA, or each
+//      scatter CTA for its own tile when the count table is small);
 //   3. per tile, each row's rank among equal keys in the tile (warp match + per-warp
 //      counts, so the order is stable in f) gives its position p; perm, inv_perm and the
-//      gathered row xp[p] = x[f / k] are written.
+//      gathered row xp[p] = x[f / k] are written.  kSub CTAs share a tile: each recomputes
+//      the tile's positions (cheap) and copies its own slice of the rows, so the row copy --
+//      the bulk of the bytes -- runs on many SMs.
+#include <type_traits>
+
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -17,6 +22,8 @@ namespace {
 
 constexpr int kTile = 256;
 constexpr int kMaxE = 256;
+constexpr int kSub = 32;  // CTAs per tile in the scatter (each copies kTile / kSub rows: one per warp)
+constexpr int kFusedScanMax = 16384;   // tile-count entries up to which the scatter does the scan
 
 __global__ void __launch_bounds__(kTile) count_kernel(const int32_t *__restrict__ ids, int64_t R,
                                                       int E, int32_t *__restrict__ tile_counts) {
@@ -32,41 +39,114 @@ __global__ void __launch_bounds__(kTile) count_kernel(const int32_t *__restrict_
   for (int e = threadIdx.x; e < E; e += kTile) tile_counts[int64_t(blockIdx.x) * E + e] = cnt[e];
 }
 
-// One CTA of kMaxE threads; thread e walks the tiles of expert e.
+// One CTA of kMaxE threads; thread e walks the tiles of expert e (loads batched so they are
+// in flight together), then the expert totals are scanned and the bases written once.
 __global__ void __launch_bounds__(kMaxE) scan_kernel(const int32_t *__restrict__ tile_counts,
                                                      int ntiles, int E, int32_t *__restrict__ tile_base,
                                                      int32_t *__restrict__ offsets) {
   __shared__ int scratch[32];
   const int e = threadIdx.x;
   int total = 0;
-  if (e < E)
-    for (int t = 0; t < ntiles; ++t) {
-      tile_base[int64_t(t) * E + e] = total;
-      total += tile_counts[int64_t(t) * E + e];
+  if (e < E) {
+    int t = 0;
+    for (; t + 8 <= ntiles; t += 8) {
+      int c[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) c[u] = tile_counts[int64_t(t + u) * E + e];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) total += c[u];
     }
+    for (; t < ntiles; ++t) total += tile_counts[int64_t(t) * E + e];
+  }
   int start = 0;
   const int all = block_exclusive_scan(e < E ? total : 0, &start, scratch);
   if (e < E) {
     offsets[e] = start;
-    for (int t = 0; t < ntiles; ++t) tile_base[int64_t(t) * E + e] += start;
+    int run = start;
+    int t = 0;
+    for (; t + 8 <= ntiles; t += 8) {
+      int c[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) c[u] = tile_counts[int64_t(t + u) * E + e];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        tile_base[int64_t(t + u) * E + e] = run;
+        run += c[u];
+      }
+    }
+    for (; t < ntiles; ++t) {
+      tile_base[int64_t(t) * E + e] = run;
+      run += tile_counts[int64_t(t) * E + e];
+    }
   }
   if (e == 0) offsets[E] = all;
 }
 
+// Copy one row: the lane's pieces are all loaded before any is stored (the loads of a row are
+// in flight together).
+template <int VEC_BYTES>
+__device__ __forceinline__ void copy_row(const uint8_t *src, uint8_t *dst, int64_t row_bytes, int lane) {
+  using V = typename std::conditional<VEC_BYTES == 16, uint4, uint2>::type;
+  constexpr int kBatch = 4;
+  for (int64_t c0 = int64_t(lane) * VEC_BYTES; c0 < row_bytes; c0 += int64_t(kBatch) * 32 * VEC_BYTES) {
+    V v[kBatch];
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int64_t c = c0 + int64_t(b) * 32 * VEC_BYTES;
+      if (c < row_bytes) v[b] = *reinterpret_cast<const V *>(src + c);
+    }
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int64_t c = c0 + int64_t(b) * 32 * VEC_BYTES;
+      if (c < row_bytes) *reinterpret_cast<V *>(dst + c) = v[b];
+    }
+  }
+}
+
+// tile_base == nullptr: the CTA derives its tile's bases from all tile counts itself (expert
+// totals and the counts of earlier tiles, summed with shared-memory integer atomics, so the
+// result does not depend on their order) and CTA 0 writes the expert offsets; used when the
+// count table is small, which saves the scan launch.
 template <int VEC_BYTES>
 __global__ void __launch_bounds__(kTile) scatter_kernel(const int32_t *__restrict__ ids,
+                                                        const int32_t *__restrict__ tile_counts,
                                                         const int32_t *__restrict__ tile_base,
-                                                        const uint8_t *__restrict__ x, int64_t R,
+                                                        int ntiles, const uint8_t *__restrict__ x, int64_t R,
                                                         int E, int k, int64_t row_bytes,
+                                                        int32_t *__restrict__ offsets,
                                                         int32_t *__restrict__ perm,
                                                         int32_t *__restrict__ inv_perm,
                                                         uint8_t *__restrict__ xp) {
   __shared__ int wcount[kTile / 32][kMaxE];
   __shared__ int dest[kTile];
+  __shared__ int tot[kMaxE], pre[kMaxE];
+  __shared__ int scratch[32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int tile = blockIdx.x / kSub, sub = blockIdx.x % kSub;
   for (int i = threadIdx.x; i < (kTile / 32) * E; i += kTile) wcount[i / E][i % E] = 0;
+  if (tile_base == nullptr)
+    for (int e = threadIdx.x; e < E; e += kTile) tot[e] = pre[e] = 0;
   __syncthreads();
-  const int64_t f = int64_t(blockIdx.x) * kTile + threadIdx.x;
+  if (tile_base == nullptr) {
+    for (int i = threadIdx.x; i < ntiles * E; i += kTile) {
+      const int t = i / E, e = i % E;
+      const int c = tile_counts[i];
+      if (c) {
+        atomicAdd(&tot[e], c);
+        if (t < tile) atomicAdd(&pre[e], c);
+      }
+    }
+    __syncthreads();
+    int start = 0;
+    const int v = threadIdx.x < E ? tot[threadIdx.x] : 0;   // E <= kMaxE == kTile
+    const int all = block_exclusive_scan(v, &start, scratch);
+    if (threadIdx.x < E) {
+      pre[threadIdx.x] += start;   // base of (this tile, expert)
+      if (blockIdx.x == 0) offsets[threadIdx.x] = start;
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) offsets[E] = all;
+  }
+  const int64_t f = int64_t(tile) * kTile + threadIdx.x;
   int e = f < R ? ids[f] : -1;
   if (e >= E) e = -1;
   const unsigned same = __match_any_sync(0xffffffffu, e);
@@ -75,30 +155,24 @@ __global__ void __launch_bounds__(kTile) scatter_kernel(const int32_t *__restric
   __syncthreads();
   dest[threadIdx.x] = -1;
   if (e >= 0) {
-    int p = tile_base[int64_t(blockIdx.x) * E + e] + rank_in_warp;
+    int p = (tile_base ? tile_base[int64_t(tile) * E + e] : pre[e]) + rank_in_warp;
     for (int w = 0; w < warp; ++w) p += wcount[w][e];
-    perm[p] = int32_t(f);
-    inv_perm[f] = p;
+    if (sub == 0) {
+      perm[p] = int32_t(f);
+      inv_perm[f] = p;
+    }
     dest[threadIdx.x] = p;
   }
   __syncthreads();
-  // gather rows: one warp per row, VEC_BYTES per lane per step
-  const int64_t base = int64_t(blockIdx.x) * kTile;
+  // gather this CTA's slice of the tile's rows: one warp per row
+  const int64_t base = int64_t(tile) * kTile;
   const int nrows = int(R - base < kTile ? R - base : kTile);
-  for (int r = warp; r < nrows; r += kTile / 32) {
+  const int r_end = min(nrows, (sub + 1) * (kTile / kSub));
+  for (int r = sub * (kTile / kSub) + warp; r < r_end; r += kTile / 32) {
     if (dest[r] < 0) continue;  // row with an out-of-range id has no position
-    const int64_t src_row = (base + r) / k;
-    const uint8_t *src = x + src_row * row_bytes;
-    uint8_t *dst = xp + int64_t(dest[r]) * row_bytes;
-    for (int64_t c = int64_t(lane) * VEC_BYTES; c < row_bytes; c += 32 * VEC_BYTES) {
-      if constexpr (VEC_BYTES == 16)
-        *reinterpret_cast<uint4 *>(dst + c) = *reinterpret_cast<const uint4 *>(src + c);
-      else
-        *reinterpret_cast<uint2 *>(dst + c) = *reinterpret_cast<const uint2 *>(src + c);
-    }
+    copy_row<VEC_BYTES>(x + ((base + r) / k) * row_bytes, xp + int64_t(dest[r]) * row_bytes, row_bytes, lane);
   }
 }
-
 
 // Whole permute in one CTA for small batches (R <= 1024 rows, decode steps): per-warp counts,
 // prefix over warps and experts, stable ranks from warp matches, then the row gather; one
@@ -152,16 +226,17 @@ __global__ void __launch_bounds__(kSmall) permute_small_kernel(const int32_t *__
     if (dest[r] < 0) continue;
     const uint8_t *src = x + int64_t(r / k) * row_bytes;
     uint8_t *dst = xp + int64_t(dest[r]) * row_bytes;
-    for (int64_t c = int64_t(lane) * VEC_BYTES; c < row_bytes; c += 32 * VEC_BYTES) {
-      if constexpr (VEC_BYTES == 16)
-        *reinterpret_cast<uint4 *>(dst + c) = *reinterpret_cast<const uint4 *>(src + c);
-      else
-        *reinterpret_cast<uint2 *>(dst + c) = *reinterpret_cast<const uint2 *>(src + c);
-    }
+    copy_row<VEC_BYTES>(src, dst, row_bytes, lane);
   }
 }
 
 }  // namespace
+
+int permute_launches(int64_t R, int64_t E) {
+  if (R <= kSmall) return 1;
+  return cdiv(R, kTile) * E <= kFusedScanMax ? 2 : 3;
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -208,12 +283,16 @@ extern "C" int moe_permute(const int32_t *ids, const void *x, int x_dtype, int64
   int32_t *tile_base = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) +
                                                    align256(size_t(ntiles) * size_t(E) * 4));
   count_kernel<<<ntiles, kTile, 0, st>>>(ids, R, int(E), tile_counts);
-  scan_kernel<<<1, kMaxE, 0, st>>>(tile_counts, ntiles, int(E), tile_base, offsets);
+  const bool fused = int64_t(ntiles) * E <= kFusedScanMax;
+  if (!fused) scan_kernel<<<1, kMaxE, 0, st>>>(tile_counts, ntiles, int(E), tile_base, offsets);
+  const int32_t *tb = fused ? nullptr : tile_base;
+  const uint8_t *xb = static_cast<const uint8_t *>(x);
+  uint8_t *xpb = static_cast<uint8_t *>(xp);
   if (row_bytes % 16 == 0)
-    scatter_kernel<16><<<ntiles, kTile, 0, st>>>(ids, tile_base, static_cast<const uint8_t *>(x), R,
-                                                 int(E), k, row_bytes, perm, inv_perm, static_cast<uint8_t *>(xp));
+    scatter_kernel<16><<<ntiles * kSub, kTile, 0, st>>>(ids, tile_counts, tb, ntiles, xb, R, int(E), k, row_bytes,
+                                                        offsets, perm, inv_perm, xpb);
   else
-    scatter_kernel<8><<<ntiles, kTile, 0, st>>>(ids, tile_base, static_cast<const uint8_t *>(x), R,
-                                                int(E), k, row_bytes, perm, inv_perm, static_cast<uint8_t *>(xp));
+    scatter_kernel<8><<<ntiles * kSub, kTile, 0, st>>>(ids, tile_counts, tb, ntiles, xb, R, int(E), k, row_bytes,
+                                                       offsets, perm, inv_perm, xpb);
   return check_launch("permute");
 }

@@ -133,13 +133,14 @@ __global__ void __launch_bounds__(kThreads) route_f32_kernel(const T *__restrict
 
 // ---- split-K router: partial logits per (K split, token, expert), then a fixed-order reduce ----
 // CTA = 64 tokens (4 warps x m16) x one K range; the router weights are staged row-major with
-// plain coalesced loads and turned into MMA B pairs by 16-bit shared-memory reads.  Decode
-// batches (a handful of tokens) spread the d x E weight read over many CTAs this way.
+// plain coalesced loads and turned into MMA B pairs by transposing ldmatrix reads; each chunk's
+// global loads are issued while the previous chunk is multiplied.  Decode batches (a handful of
+// tokens) spread the d x E weight read over many CTAs this way.
 constexpr int kPTok = 64;
 constexpr int kPKC = 64;
-constexpr int kPEG = 64;   // experts per pass
+// experts per pass (kPEG): 32 when E <= 32 (half the accumulators), else 64
 
-template <typename T>
+template <typename T, int kPEG>
 __global__ void __launch_bounds__(kThreads) route_partial_kernel(const T *__restrict__ x, const T *__restrict__ wr,
                                                                  int T_, int d, int E, int KS,
                                                                  float *__restrict__ part) {
@@ -160,39 +161,55 @@ __global__ void __launch_bounds__(kThreads) route_partial_kernel(const T *__rest
     for (int i = 0; i < kPEG / 8; ++i)
 #pragma unroll
       for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-    for (int k0 = k_begin; k0 < k_end; k0 += kPKC) {
+    // chunk loads go to registers first: the next chunk's loads are in flight while the
+    // current one is multiplied
+    constexpr int kXPer = kPTok * (kPKC / 8) / kThreads;   // 16-byte pieces of x per thread
+    constexpr int kWPer = kPKC * kPEG / 2 / kThreads;       // 32-bit words of Wr per thread
+    uint4 xr[kXPer];
+    uint32_t wr2[kWPer];
+    const bool even_e = (E & 1) == 0;
+    auto load_chunk = [&](int k0) {
       const int kc = min(kPKC, k_end - k0);
-      for (int i = tid; i < kPTok * (kPKC / 8); i += kThreads) {
+#pragma unroll
+      for (int j = 0; j < kXPer; ++j) {
+        const int i = tid + j * kThreads;
         const int r = i / (kPKC / 8), c8 = (i % (kPKC / 8)) * 8;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (tok0 + r < T_ && c8 < kc) v = *reinterpret_cast<const uint4 *>(xg + int64_t(tok0 + r) * d + k0 + c8);
-        *reinterpret_cast<uint4 *>(&xs[r][c8]) = v;
+        xr[j] = (tok0 + r < T_ && c8 < kc) ? *reinterpret_cast<const uint4 *>(xg + int64_t(tok0 + r) * d + k0 + c8)
+                                           : make_uint4(0, 0, 0, 0);
       }
-      if ((E & 1) == 0) {
-        // 32-bit words of the (kc x EG) block: every load is issued before any store
-        constexpr int kPer = kPKC * kPEG / 2 / kThreads;
-        uint32_t v[kPer];
+      if (even_e) {
 #pragma unroll
-        for (int j = 0; j < kPer; ++j) {
+        for (int j = 0; j < kWPer; ++j) {
           const int i = tid + j * kThreads;
           const int kk = i / (kPEG / 2), ew = i % (kPEG / 2);
-          v[j] = (kk < kc && 2 * ew < EG)
-                     ? *reinterpret_cast<const uint32_t *>(wg + int64_t(k0 + kk) * E + g0 + 2 * ew)
-                     : 0u;
+          wr2[j] = (kk < kc && 2 * ew < EG) ? *reinterpret_cast<const uint32_t *>(wg + int64_t(k0 + kk) * E + g0 + 2 * ew)
+                                            : 0u;
         }
+      } else {   // odd E: 16-bit reads, packed into the same words
 #pragma unroll
-        for (int j = 0; j < kPer; ++j) {
+        for (int j = 0; j < kWPer; ++j) {
           const int i = tid + j * kThreads;
           const int kk = i / (kPEG / 2), ew = i % (kPEG / 2);
-          *reinterpret_cast<uint32_t *>(&ws[kk][2 * ew]) = v[j];
+          const uint32_t lo = (kk < kc && 2 * ew < EG) ? wg[int64_t(k0 + kk) * E + g0 + 2 * ew] : 0u;
+          const uint32_t hi = (kk < kc && 2 * ew + 1 < EG) ? wg[int64_t(k0 + kk) * E + g0 + 2 * ew + 1] : 0u;
+          wr2[j] = lo | (hi << 16);
         }
-      } else {
-        for (int i = tid; i < kPKC * kPEG; i += kThreads) {
-          const int kk = i / kPEG, e = i % kPEG;
-          ws[kk][e] = (kk < kc && e < EG) ? wg[int64_t(k0 + kk) * E + g0 + e] : uint16_t(0);
-        }
+      }
+    };
+    if (k_begin < k_end) load_chunk(k_begin);
+    for (int k0 = k_begin; k0 < k_end; k0 += kPKC) {
+#pragma unroll
+      for (int j = 0; j < kXPer; ++j) {
+        const int i = tid + j * kThreads;
+        *reinterpret_cast<uint4 *>(&xs[i / (kPKC / 8)][(i % (kPKC / 8)) * 8]) = xr[j];
+      }
+#pragma unroll
+      for (int j = 0; j < kWPer; ++j) {
+        const int i = tid + j * kThreads;
+        *reinterpret_cast<uint32_t *>(&ws[i / (kPEG / 2)][2 * (i % (kPEG / 2))]) = wr2[j];
       }
       __syncthreads();
+      if (k0 + kPKC < k_end) load_chunk(k0 + kPKC);
 #pragma unroll
       for (int ks = 0; ks < kPKC / 16; ++ks) {
         const int c = ks * 16 + 2 * t;
@@ -201,13 +218,20 @@ __global__ void __launch_bounds__(kThreads) route_partial_kernel(const T *__rest
         a[1] = *reinterpret_cast<const uint32_t *>(&xs[warp * 16 + g + 8][c]);
         a[2] = *reinterpret_cast<const uint32_t *>(&xs[warp * 16 + g][c + 8]);
         a[3] = *reinterpret_cast<const uint32_t *>(&xs[warp * 16 + g + 8][c + 8]);
+        // B pairs of two n8 tiles from the row-major (k, e) block: one transposing ldmatrix;
+        // lanes 0-7 / 8-15 / 16-23 / 24-31 address rows k0..7 / k8..15 of experts e0.. / e0+8..
 #pragma unroll
-        for (int nt = 0; nt < kPEG / 8; ++nt) {
-          if (nt < ntiles) {
-            const int e = nt * 8 + g;
-            const uint32_t b0 = uint32_t(ws[c][e]) | (uint32_t(ws[c + 1][e]) << 16);
-            const uint32_t b1 = uint32_t(ws[c + 8][e]) | (uint32_t(ws[c + 9][e]) << 16);
-            mma16816(acc[nt], a, b0, b1, T());
+        for (int np = 0; np < kPEG / 16; ++np) {
+          if (2 * np < ntiles) {
+            const int krow = ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+            const int ecol = np * 16 + (lane >> 4) * 8;
+            const uint32_t addr = static_cast<uint32_t>(__cvta_generic_to_shared(&ws[krow][ecol]));
+            uint32_t b[4];
+            asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                         : "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3])
+                         : "r"(addr));
+            mma16816(acc[2 * np], a, b[0], b[1], T());
+            if (2 * np + 1 < ntiles) mma16816(acc[2 * np + 1], a, b[2], b[3], T());
           }
         }
       }
@@ -243,15 +267,14 @@ __global__ void __launch_bounds__(kThreads) route_reduce_topk_kernel(const float
   for (int e = lane; e < E; e += 32) {
     const float *pe = part + int64_t(tok) * E + e;
     float v = 0.f;
-    int s = 0;
-    for (; s + 8 <= S; s += 8) {   // eight independent loads in flight, summed in split order
+    for (int s = 0; s < S; s += 8) {   // up to eight loads in flight, summed in split order
       float q[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) q[u] = pe[(s + u) * sstride];
+      for (int u = 0; u < 8; ++u) q[u] = s + u < S ? pe[(s + u) * sstride] : 0.f;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) v += q[u];
+      for (int u = 0; u < 8; ++u)
+        if (s + u < S) v += q[u];
     }
-    for (; s < S; ++s) v += pe[s * sstride];
     lg[warp][e] = v + (bias ? bias[e] : 0.f);
   }
   __syncwarp();
@@ -311,12 +334,16 @@ extern "C" int moe_route_topk(const void *x, int x_dtype, const void *w_router, 
     const int KS = int(cdiv(cdiv(d, kPKC), S) * kPKC);
     float *part = static_cast<float *>(workspace);
     const dim3 pgrid(unsigned(cdiv(T, kPTok)), unsigned(S));
-    if (x_dtype == MOE_F16)
-      route_partial_kernel<__half><<<pgrid, kThreads, 0, st>>>(static_cast<const __half *>(x),
-          static_cast<const __half *>(w_router), int(T), int(d), int(E), KS, part);
-    else
-      route_partial_kernel<__nv_bfloat16><<<pgrid, kThreads, 0, st>>>(static_cast<const __nv_bfloat16 *>(x),
-          static_cast<const __nv_bfloat16 *>(w_router), int(T), int(d), int(E), KS, part);
+    const bool narrow = E <= 32;
+    if (x_dtype == MOE_F16) {
+      const __half *xh = static_cast<const __half *>(x), *wh = static_cast<const __half *>(w_router);
+      if (narrow) route_partial_kernel<__half, 32><<<pgrid, kThreads, 0, st>>>(xh, wh, int(T), int(d), int(E), KS, part);
+      else route_partial_kernel<__half, 64><<<pgrid, kThreads, 0, st>>>(xh, wh, int(T), int(d), int(E), KS, part);
+    } else {
+      const __nv_bfloat16 *xb = static_cast<const __nv_bfloat16 *>(x), *wb = static_cast<const __nv_bfloat16 *>(w_router);
+      if (narrow) route_partial_kernel<__nv_bfloat16, 32><<<pgrid, kThreads, 0, st>>>(xb, wb, int(T), int(d), int(E), KS, part);
+      else route_partial_kernel<__nv_bfloat16, 64><<<pgrid, kThreads, 0, st>>>(xb, wb, int(T), int(d), int(E), KS, part);
+    }
     MOE_TRY(check_launch("route_partial"));
     route_reduce_topk_kernel<<<unsigned(cdiv(T, kThreads / 32)), kThreads, 0, st>>>(part, S, int(T), int(E), bias, k,
                                                                                  renormalize, ids, gate_w);
