@@ -386,3 +386,25 @@ def test_tcgen05_gemm_repeatable(M):
         again = M.grouped_gemm(a, packed, cfg.bits, E, K, N, cfg.group, off, "none", torch.float32)
         assert torch.equal(again, first)
     assert M.device_error(DEV) == 0
+
+
+@pytest.mark.parametrize("R", [16, 48, 1024])
+def test_gelu_epilogue_accuracy(M, R):
+    """out[r, n] = GELU(x_r) through each GEMM path (one weight of 1, fp32 output): the kernels'
+    GELU against the float64 erf form within 1e-6 * max(1, |x|)."""
+    E, K, N = 1, 128, 128
+    x = torch.linspace(-9.0, 9.0, R).to(torch.float16)
+    a = torch.zeros((R, K), dtype=torch.float16)
+    a[:, 0] = x
+    q = torch.zeros((E, K, N), dtype=torch.int8)
+    q[0, 0, :] = 1
+    s = torch.ones((E, 1, N), dtype=torch.float16)
+    packed = M.pack_weights(q.to(DEV), s.to(DEV), 4, 0)
+    off = torch.tensor([0, R], dtype=torch.int32)
+    path = M.gemm_path(R, E, K, N, 4, 0, "gelu")
+    assert path == {16: "gemv", 48: "mma", 1024: "tcgen05"}[R]
+    got = M.grouped_gemm(a.to(DEV), packed, 4, E, K, N, 0, off.to(DEV), "gelu", torch.float32).cpu().double()
+    assert M.device_error(DEV) == 0
+    ref = O.gelu(x.double())[:, None].expand(R, N)
+    err = (got - ref).abs() / x.double().abs().clamp(min=1.0)[:, None]
+    assert err.max().item() <= 1e-6, (path, err.max().item())

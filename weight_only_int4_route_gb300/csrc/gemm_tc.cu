@@ -129,6 +129,14 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
       : "memory");
 }
 
+// Bring a weight box into L2 ahead of its shared-memory copy (no barrier, no shared memory).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];\n" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
 
@@ -331,6 +339,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kProdWarp) {
     // ------------------------------------------------ producer (TMA)
     if (lane == 0) {
+      // rolling L2 prefetch of the weight blocks kPrefetch K blocks ahead of the stage copies (into
+      // the CTA's next tile), so a stage copy waits on L2 rather than DRAM
+      constexpr int kPrefetch = 8;
+      int pf_tile = blockIdx.x, pf_kb = 0, pf_A = 0, pf_B = 0;
+      auto pf_rows = [&]() {
+        const Tile tn = decode_tile(pf_tile, s_tstart, s_off, E, p.ncb);
+        pf_A = tn.e * p.N + (p.swiglu ? tn.cb * (kBM / 2) : tn.cb * kBM);
+        pf_B = p.swiglu ? tn.e * p.N + (p.N >> 1) + tn.cb * (kBM / 2) : pf_A + kBM / 2;
+      };
+      auto pf_step = [&]() {   // prefetch the block at the cursor, then advance it
+        if (pf_tile >= total_tiles) return;
+        tma_prefetch_2d(&map_w, pf_kb * kWords, pf_A);
+        tma_prefetch_2d(&map_w, pf_kb * kWords, pf_B);
+        if (++pf_kb == nkb) {
+          pf_kb = 0;
+          pf_tile += gridDim.x;
+          if (pf_tile < total_tiles) pf_rows();
+        }
+      };
+      if (pf_tile < total_tiles) pf_rows();
+      for (int i = 0; i < kPrefetch; ++i) pf_step();
       uint32_t it = 0;
       int issued[kStages];
 #pragma unroll
@@ -352,6 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(sW + s * kWBytes, &map_w, kb * kWords, rowA, &full[s]);
           tma_load_2d(sW + s * kWBytes + kWBytes / 2, &map_w, kb * kWords, rowB, &full[s]);
           issued[s] = int((it / kStages) & 1) + 1;  // parity of this fill, +1
+          pf_step();
         }
       }
       // drain: every issued copy has landed before the CTA may exit
@@ -382,11 +412,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t b_addr = su32(sB + s * kBBytes);
+          // descriptor of the stage built once; MMA j adds its start offset (16-byte units, no
+          // carry out of the 14-bit field: shared addresses stay below 256 KB)
+          const uint64_t bd0 = sw128_desc(su32(sB + s * kBBytes));
           const uint32_t a_col = tmem + kACol0 + uint32_t(s) * kAStageCols;
 #pragma unroll
           for (int j = 0; j < kBK / 16; ++j) {
-            const uint64_t bd = sw128_desc(b_addr + (j >> 2) * kBHalf + (j & 3) * 32);
+            const uint64_t bd = bd0 + uint64_t(((j >> 2) * kBHalf + (j & 3) * 32) >> 4);
             tc_mma_ts(d_tmem, a_col + uint32_t(j * 8), bd, idesc, (kb | j) != 0);
           }
           tc_commit(&freeb[s]);
