@@ -57,9 +57,10 @@ def test_static_scratch_matches_workspace_entry(M, which):
 
 
 def test_static_scratch_refuses_oversize(M):
-    # one expert with 60 rows and a long reduction: the planner splits K 4 ways and the
-    # partial sums (4 x 60 x 4096 fp32) exceed the 2 MiB array
-    R, E, K, N = 60, 1, 8192, 4096
+    # one expert with 60 rows, a long reduction and a channel count the tensor-memory kernel
+    # does not take (not a multiple of 128): the warp-MMA plan splits K and its fp32 partial
+    # sums (splits x 60 x 4160) exceed the 2 MiB array
+    R, E, K, N = 60, 1, 8192, 4160
     need = M.lib().moe_grouped_gemm_workspace_size(R, E, K, N, 4, 0)
     assert need > (2 << 20)
     nul = ctypes.c_void_p(16)   # never dereferenced: the call is refused on the host

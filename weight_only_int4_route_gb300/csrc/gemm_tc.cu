@@ -620,18 +620,20 @@ int launch_typed(const GemmArgs &g, cudaStream_t st) {
 
 }  // namespace
 
-bool tc_supported(const GemmArgs &g) {
-  if (g.bits != 4 && g.bits != 8) return false;
-  if (g.offsets == nullptr) return false;
-  if (g.K % kBK != 0) return false;
-  if (g.act == MOE_ACT_SWIGLU) {
-    if ((g.N / 2) % (kBM / 2) != 0) return false;
-  } else if (g.N % kBM != 0) {
+bool tc_shape_ok(int64_t E, int64_t K, int64_t N, int bits, int group, int act) {
+  if (bits != 4 && bits != 8) return false;
+  if (K % kBK != 0) return false;
+  if (act == MOE_ACT_SWIGLU) {
+    if ((N / 2) % (kBM / 2) != 0) return false;
+  } else if (N % kBM != 0) {
     return false;
   }
-  if (g.group != 0 && g.group % kBK != 0) return false;
-  if (int64_t(g.E) * g.N >= (int64_t(1) << 31)) return false;
-  return true;
+  if (group != 0 && group % kBK != 0) return false;
+  return E * N < (int64_t(1) << 31);
+}
+
+bool tc_supported(const GemmArgs &g) {
+  return g.offsets != nullptr && tc_shape_ok(g.E, g.K, g.N, g.bits, g.group, g.act);
 }
 
 int launch_gemm_tc(const GemmArgs &g, cudaStream_t st) {

@@ -83,6 +83,8 @@ int launch_gemm(const GemmArgs &g, const GemmPlan &pl, cudaStream_t st);
 int launch_gemm_mma(const GemmArgs &g, const GemmPlan &pl, cudaStream_t st);
 int launch_gemv(const GemmArgs &g, const GemmPlan &pl, cudaStream_t st);
 bool tc_supported(const GemmArgs &g);
+// Shapes the tcgen05 kernel takes (the launch also needs an offsets array).
+bool tc_shape_ok(int64_t E, int64_t K, int64_t N, int bits, int group, int act);
 int launch_gemm_tc(const GemmArgs &g, cudaStream_t st);
 int read_device_error(cudaStream_t st, int *out);
 // Kernel launches of one moe_permute call for R rows over E experts.
