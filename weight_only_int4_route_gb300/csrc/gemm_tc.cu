@@ -54,13 +54,13 @@ constexpr int kThreads = (kDqWarp0 + 4 * kDqGroups) * 32;
 constexpr int kBM = 128;          // output channels per tile (MMA M)
 constexpr int kBN = 128;          // rows per tile (MMA N upper bound)
 constexpr int kBK = 128;          // K per pipeline stage
-constexpr int kStages = 4;        // pipeline stages (shared memory and TMEM A)
+constexpr int kStagesQ = 4;       // pipeline stages (shared memory and TMEM A), quantized weights
 // Every fill of a stage must go to the same dequant group.  A group waits on full[s] by phase
 // parity, which cannot tell "one phase ahead" from "complete": with groups taking K blocks
 // round-robin over a stage count they do not divide, the group of fill it + kStages could reach
 // full[s] while fill it (another group's) was still in flight -- TMA completions of different
 // stages are not ordered -- and pass the wait at once.
-static_assert(kStages % kDqGroups == 0, "each stage must belong to one dequant group");
+static_assert(kStagesQ % kDqGroups == 0, "each stage must belong to one dequant group");
 constexpr int kMaxE = 256;
 constexpr int kBHalf = kBN * 64 * 2;         // one 64-wide swizzle atom column block: 16 KB
 constexpr int kBBytes = 2 * kBHalf;          // activation stage: 32 KB
@@ -71,9 +71,13 @@ constexpr long long kTimeoutCycles = 4000000000LL;  // ~2 s at 2 GHz
 
 enum : int { kErrTimeoutFull = 1, kErrTimeoutFree = 2, kErrTimeoutReady = 3, kErrTimeoutD = 4, kErrTimeoutDrain = 5 };
 
+// 4/8-bit: packed words (SWIZZLE_NONE boxes), dequantized into TMEM.  16-bit: the weights are
+// the A operand as they are, TMA-loaded with the same 128-byte swizzle as the activations and
+// read by the MMA from shared memory (no dequant work); a stage is then 64 KB, so three stages.
 template <int BITS> struct WB {
   static constexpr int kWordsPerRow = kBK * BITS / 32;    // u32 words per channel per stage
   static constexpr int kBytes = kBM * kWordsPerRow * 4;   // weight stage bytes
+  static constexpr int kStages = BITS == 16 ? 3 : kStagesQ;
 };
 
 struct TcParams {
@@ -151,6 +155,16 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// A from shared memory (16-bit weights)
+__device__ __forceinline__ void tc_mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -238,7 +252,7 @@ __device__ __forceinline__ void epilogue_cols(const TcParams &p, const Tile &t, 
   int ch;
   if (p.swiglu) ch = r < kBM / 2 ? t.cb * (kBM / 2) + r : (p.N >> 1) + t.cb * (kBM / 2) + (r - kBM / 2);
   else ch = t.cb * kBM + r;
-  const float sc = p.group == 0 ? ldscale<T>(p.scales, int64_t(t.e) * p.N + ch) : 1.0f;
+  const float sc = (p.group == 0 && p.scales) ? ldscale<T>(p.scales, int64_t(t.e) * p.N + ch) : 1.0f;
   const int Nout = p.swiglu ? (p.N >> 1) : p.N;
   for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
     float v[32];
@@ -282,6 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const TcParams p) {
   constexpr int kWBytes = WB<BITS>::kBytes;
   constexpr int kWords = WB<BITS>::kWordsPerRow;
+  constexpr int kStages = WB<BITS>::kStages;
   extern __shared__ __align__(1024) uint8_t dsmem[];
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dsmem) + 1023) & ~uintptr_t(1023));
   uint8_t *sB = base;                                   // kStages x 32 KB (two 1024-aligned 16 KB halves)
@@ -320,8 +335,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::);
   }
   int cnt = 0;
-  if (tid < E) {
-    const int o0 = p.offsets[tid], o1 = p.offsets[tid + 1];
+  if (tid < E) {   // no offsets array: one expert owning all R rows
+    const int o0 = p.offsets ? p.offsets[tid] : 0, o1 = p.offsets ? p.offsets[tid + 1] : p.R;
     cnt = ((o1 - o0 + kBN - 1) / kBN) * p.ncb;
     s_off[tid] = o0;
     if (tid == E - 1) s_off[E] = o1;
@@ -350,8 +365,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto pf_step = [&]() {   // prefetch the block at the cursor, then advance it
         if (pf_tile >= total_tiles) return;
-        tma_prefetch_2d(&map_w, pf_kb * kWords, pf_A);
-        tma_prefetch_2d(&map_w, pf_kb * kWords, pf_B);
+        if constexpr (BITS == 16) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            tma_prefetch_2d(&map_w, pf_kb * kBK + 64 * h, pf_A);
+            tma_prefetch_2d(&map_w, pf_kb * kBK + 64 * h, pf_B);
+          }
+        } else {
+          tma_prefetch_2d(&map_w, pf_kb * kWords, pf_A);
+          tma_prefetch_2d(&map_w, pf_kb * kWords, pf_B);
+        }
         if (++pf_kb == nkb) {
           pf_kb = 0;
           pf_tile += gridDim.x;
@@ -378,8 +401,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_expect_tx(&full[s], kBBytes + kWBytes);
           tma_load_2d(sB + s * kBBytes, &map_x, kb * kBK, t.row0, &full[s]);
           tma_load_2d(sB + s * kBBytes + kBHalf, &map_x, kb * kBK + 64, t.row0, &full[s]);
-          tma_load_2d(sW + s * kWBytes, &map_w, kb * kWords, rowA, &full[s]);
-          tma_load_2d(sW + s * kWBytes + kWBytes / 2, &map_w, kb * kWords, rowB, &full[s]);
+          if constexpr (BITS == 16) {   // K halves of 16 KB; rows 0-63 (rowA..) then 64-127 (rowB..)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              tma_load_2d(sW + s * kWBytes + h * kBHalf, &map_w, kb * kBK + 64 * h, rowA, &full[s]);
+              tma_load_2d(sW + s * kWBytes + h * kBHalf + kBHalf / 2, &map_w, kb * kBK + 64 * h, rowB, &full[s]);
+            }
+          } else {
+            tma_load_2d(sW + s * kWBytes, &map_w, kb * kWords, rowA, &full[s]);
+            tma_load_2d(sW + s * kWBytes + kWBytes / 2, &map_w, kb * kWords, rowB, &full[s]);
+          }
           issued[s] = int((it / kStages) & 1) + 1;  // parity of this fill, +1
           pf_step();
         }
@@ -407,7 +438,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t d_tmem = tmem + uint32_t(db * kBN);
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % kStages;
-          if (!mbar_wait(&ready[s], (it / kStages) & 1, abort_flag, kErrTimeoutReady)) {
+          // 16-bit weights are MMA-ready once the copies land; else the dequant group signals
+          if (!(BITS == 16 ? mbar_wait(&full[s], (it / kStages) & 1, abort_flag, kErrTimeoutFull)
+                           : mbar_wait(&ready[s], (it / kStages) & 1, abort_flag, kErrTimeoutReady))) {
             ok = false;
             break;
           }
@@ -416,10 +449,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           // carry out of the 14-bit field: shared addresses stay below 256 KB)
           const uint64_t bd0 = sw128_desc(su32(sB + s * kBBytes));
           const uint32_t a_col = tmem + kACol0 + uint32_t(s) * kAStageCols;
+          const uint64_t ad0 = BITS == 16 ? sw128_desc(su32(sW + s * kWBytes)) : 0;
 #pragma unroll
           for (int j = 0; j < kBK / 16; ++j) {
-            const uint64_t bd = bd0 + uint64_t(((j >> 2) * kBHalf + (j & 3) * 32) >> 4);
-            tc_mma_ts(d_tmem, a_col + uint32_t(j * 8), bd, idesc, (kb | j) != 0);
+            const uint64_t off = uint64_t(((j >> 2) * kBHalf + (j & 3) * 32) >> 4);
+            if constexpr (BITS == 16) tc_mma_ss(d_tmem, ad0 + off, bd0 + off, idesc, (kb | j) != 0);
+            else tc_mma_ts(d_tmem, a_col + uint32_t(j * 8), bd0 + off, idesc, (kb | j) != 0);
           }
           tc_commit(&freeb[s]);
         }
@@ -431,6 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(drain, 0, &never, kErrTimeoutDrain);
     }
   } else if (warp >= kDqWarp0) {
+    if constexpr (BITS != 16) {   // 16-bit weights need no conversion: these warps idle
     // ------------------------------------------------ dequant -> TMEM A stages
     const int q = warp & 3;                  // TMEM lane quarter
     const int grp = (warp - kDqWarp0) >> 2;  // converts K blocks kb with kb % kDqGroups == grp
@@ -462,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {   // two 64-wide halves of the K block, 32 columns each
           uint32_t pr[32];
-          if constexpr (BITS == 4) {
+          if constexpr (BITS != 8) {   // 4-bit (16-bit never reaches the dequant warps)
             const uint4 w0 = *reinterpret_cast<const uint4 *>(wp + 32 * h);
             const uint4 w1 = *reinterpret_cast<const uint4 *>(wp + 32 * h + 16);
             const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
@@ -503,6 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&ready[s]);
       }
+    }
     }
   } else {
     // ------------------------------------------------ epilogue (warps 0-7)
@@ -557,8 +594,9 @@ EncodeTiledFn encode_fn() {
 }
 
 size_t smem_bytes(int bits) {
-  const size_t wbytes = bits == 4 ? WB<4>::kBytes : WB<8>::kBytes;
-  return 1024 /*align slack*/ + kStages * (kBBytes + wbytes) + 2 * 32 * 64 * 4 + (3 * kStages + 5) * 8 +
+  const size_t wbytes = bits == 4 ? WB<4>::kBytes : (bits == 8 ? WB<8>::kBytes : WB<16>::kBytes);
+  const int st = bits == 16 ? WB<16>::kStages : kStagesQ;
+  return 1024 /*align slack*/ + st * (kBBytes + wbytes) + 2 * 32 * 64 * 4 + (3 * st + 5) * 8 +
          (2 * (kMaxE + 1) + 32 + 2) * 4;
 }
 
@@ -577,7 +615,16 @@ int launch_typed(const GemmArgs &g, cudaStream_t st) {
                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return set_error(MOE_ERR_CUDA, "activation tensor map encode failed (%d)", int(r));
   }
-  {
+  if constexpr (BITS == 16) {   // (E*N, K) 16-bit rows, 64 x 64 boxes with the activations' swizzle
+    const cuuint64_t dims[2] = {cuuint64_t(g.K), cuuint64_t(int64_t(g.E) * g.N)};
+    const cuuint64_t strides[1] = {cuuint64_t(g.K) * 2};
+    const cuuint32_t box[2] = {64u, cuuint32_t(kBM / 2)};
+    const cuuint32_t es[2] = {1, 1};
+    const CUresult r = enc(&mw, std::is_same<T, __half>::value ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                           2, const_cast<void *>(g.w), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return set_error(MOE_ERR_CUDA, "weight tensor map encode failed (%d)", int(r));
+  } else {
     const int words_per_row = g.K * BITS / 32;
     const cuuint64_t dims[2] = {cuuint64_t(words_per_row), cuuint64_t(int64_t(g.E) * g.N)};
     const cuuint64_t strides[1] = {cuuint64_t(words_per_row) * 4};
@@ -602,8 +649,8 @@ int launch_typed(const GemmArgs &g, cudaStream_t st) {
   tp.swiglu = g.act == MOE_ACT_SWIGLU ? 1 : 0;
   tp.ncb = tp.swiglu ? g.N / kBM : g.N / kBM;  // SwiGLU: 64 gate + 64 up channels per tile
   const size_t smem = smem_bytes(BITS);
-  static bool attr_set[2][2] = {{false, false}, {false, false}};
-  bool &done = attr_set[std::is_same<T, __half>::value ? 0 : 1][BITS == 4 ? 0 : 1];
+  static bool attr_set[2][3] = {{false, false, false}, {false, false, false}};
+  bool &done = attr_set[std::is_same<T, __half>::value ? 0 : 1][BITS == 4 ? 0 : (BITS == 8 ? 1 : 2)];
   if (!done) {
     if (cudaFuncSetAttribute(gemm_tc_kernel<T, BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
         cudaSuccess)
@@ -621,7 +668,8 @@ int launch_typed(const GemmArgs &g, cudaStream_t st) {
 }  // namespace
 
 bool tc_shape_ok(int64_t E, int64_t K, int64_t N, int bits, int group, int act) {
-  if (bits != 4 && bits != 8) return false;
+  if (bits != 4 && bits != 8 && bits != 16) return false;
+  if (bits == 16 && group != 0) return false;
   if (K % kBK != 0) return false;
   if (act == MOE_ACT_SWIGLU) {
     if ((N / 2) % (kBM / 2) != 0) return false;
@@ -633,14 +681,15 @@ bool tc_shape_ok(int64_t E, int64_t K, int64_t N, int bits, int group, int act) 
 }
 
 bool tc_supported(const GemmArgs &g) {
-  return g.offsets != nullptr && tc_shape_ok(g.E, g.K, g.N, g.bits, g.group, g.act);
+  return (g.offsets != nullptr || g.E == 1) && tc_shape_ok(g.E, g.K, g.N, g.bits, g.group, g.act);
 }
 
 int launch_gemm_tc(const GemmArgs &g, cudaStream_t st) {
   if (g.R == 0) return MOE_OK;
   const bool bf = g.a_dtype == MOE_BF16;
   if (g.bits == 4) return bf ? launch_typed<__nv_bfloat16, 4>(g, st) : launch_typed<__half, 4>(g, st);
-  return bf ? launch_typed<__nv_bfloat16, 8>(g, st) : launch_typed<__half, 8>(g, st);
+  if (g.bits == 8) return bf ? launch_typed<__nv_bfloat16, 8>(g, st) : launch_typed<__half, 8>(g, st);
+  return bf ? launch_typed<__nv_bfloat16, 16>(g, st) : launch_typed<__half, 16>(g, st);
 }
 
 int read_device_error(cudaStream_t st, int *out) {
