@@ -324,8 +324,8 @@ def _check_layer(M, cfg, T, subset=None):
 
 
 @pytest.mark.parametrize("name,T", [("tiny", 16), ("tiny", 1), ("encdec_int8", 40), ("encdec_int4", 40),
-                                    ("encdec_int4", 77), ("qwen", 1), ("qwen", 8), ("qwen", 32),
-                                    ("dsv2", 32), ("phi", 1), ("phi", 16)])
+                                    ("encdec_int4", 77), ("encdec_int4", 1280), ("encdec_int8", 640),
+                                    ("qwen", 1), ("qwen", 8), ("qwen", 32), ("dsv2", 32), ("phi", 1), ("phi", 16)])
 def test_layer_matches_oracle(M, name, T):
     _check_layer(M, synth.CONFIGS[name], T)
 
@@ -407,3 +407,29 @@ def test_gelu_epilogue_accuracy(M, R, N, path):
     ref = O.gelu(x.double())[:, None].expand(R, N)
     err = (got - ref).abs() / x.double().abs().clamp(min=1.0)[:, None]
     assert err.max().item() <= 1e-6, (path, err.max().item())
+
+
+
+@pytest.mark.parametrize("name", ["encdec_int4", "encdec_int8"])
+def test_fused_top1_combine_is_bit_identical(M, name):
+    """Top-1 without a shared expert: FC2's epilogue writes the gated rows to their tokens. The
+    layer output equals, bit for bit, the separate calls: route, permute, FC1, FC2 (fp32), combine."""
+    cfg = synth.CONFIGS[name]
+    T = 1280
+    w, x = layer_inputs(cfg, T)
+    layer, out = _run_layer(M, cfg, w, x)
+    assert layer.launch_count(T) == 6    # router (2), permute (2), FC1, FC2: no combine launch
+    packed = PackedLayer_from(cfg, w)
+    xd = x.to(DEV)
+    ids, gate = M.route_topk(xd, packed.wr, None, cfg.k)
+    offs, perm, inv, xp = M.permute(ids, xd, cfg.E)
+    h = M.grouped_gemm(xp, packed.w1, cfg.bits, cfg.E, cfg.d, cfg.F1, cfg.group, offs, cfg.act, cfg.torch_dtype)
+    y = M.grouped_gemm(h, packed.w2, cfg.bits, cfg.E, cfg.F, cfg.d, cfg.group, offs, "none", torch.float32)
+    sep = M.unpermute_combine(y, inv, gate, None, cfg.torch_dtype)
+    assert M.device_error(DEV) == 0
+    assert torch.equal(out, sep)
+
+
+def PackedLayer_from(cfg, w):
+    from weight_only_int4_route_gb300.moe import PackedLayer
+    return PackedLayer.from_weights(cfg, w, DEV)

@@ -107,6 +107,7 @@ int grouped_gemm(int bits, const void *a, int a_dtype, const void *packed_w, int
 struct LayerPlan {
   int64_t T, R;
   GemmPlan fc1, fc2, sh1, sh2;
+  bool fused_combine;   // top-1, no shared expert, FC2 on tcgen05: FC2 writes the layer output
   size_t o_ids, o_gate, o_off, o_perm, o_inv, o_rws, o_pws, o_xp, o_p1, o_h, o_y, o_hs, o_ps1, o_ys, total;
 };
 
@@ -131,6 +132,10 @@ LayerPlan plan_layer(const moe_layer_desc *d, int64_t T) {
   const int64_t F1 = d->act == MOE_ACT_SWIGLU ? 2 * d->F : d->F;
   p.fc1 = plan_gemm(p.R, d->E, d->d, F1, d->bits, d->act, false);
   p.fc2 = plan_gemm(p.R, d->E, d->F, d->d, d->bits, MOE_ACT_NONE, true);
+  // one routed row per token and nothing else to add: the un-permute and gate of the combine
+  // step go into FC2's epilogue (the tcgen05 kernel's), the same arithmetic with one rounding
+  p.fused_combine = d->k == 1 && d->Fs == 0 && p.fc2.kind == kKindTc && p.fc2.splits == 1 &&
+                    tc_shape_ok(d->E, d->F, d->d, d->bits, d->group, MOE_ACT_NONE);
   size_t o = 0;
   auto take = [&](size_t bytes) {
     const size_t at = o;
@@ -293,7 +298,7 @@ extern "C" int moe_layer_routing_view(const moe_layer_desc *desc, int64_t T, voi
 extern "C" int moe_layer_launch_count(const moe_layer_desc *desc, int64_t T) {
   if (check_desc(desc) != MOE_OK || T <= 0) return 0;
   const LayerPlan p = plan_layer(desc, T);
-  int n = (desc->router_dtype == MOE_F32 ? 1 : 2) /*route*/ + permute_launches(p.R, desc->E) /*permute*/ + 1 /*fc1*/ + (p.fc1.partial ? 1 : 0) + 1 /*fc2*/ + 1 /*combine*/;
+  int n = (desc->router_dtype == MOE_F32 ? 1 : 2) /*route*/ + permute_launches(p.R, desc->E) /*permute*/ + 1 /*fc1*/ + (p.fc1.partial ? 1 : 0) + 1 /*fc2*/ + (p.fused_combine ? 0 : 1) /*combine*/;
   if (desc->Fs > 0) n += 2 + (p.sh1.partial ? 1 : 0);
   return n;
 }
@@ -352,6 +357,16 @@ extern "C" int moe_layer_forward_profiled(const moe_layer_desc *desc, const moe_
                                     h, dt, p1), p.fc1, st));
   if (p.fc1.partial) MOE_TRY(launch_reduce_act(p1, p.fc1.splits, p.R, int(F1), desc->act, h, dt, st));
   MOE_TRY(mark(MOE_STAGE_FC1));
+  if (p.fused_combine) {
+    GemmArgs g2 = make_args(desc->bits, h, dt, w->w2, E, F, d, desc->group, offs, p.R, MOE_ACT_NONE, out, dt,
+                            nullptr);
+    g2.row_dest = perm;   // k == 1: perm[p] is the token of permuted row p
+    g2.row_gate = gate;
+    MOE_TRY(launch_gemm_tc(g2, st));
+    MOE_TRY(mark(MOE_STAGE_FC2));
+    MOE_TRY(mark(MOE_STAGE_SHARED));
+    return mark(MOE_STAGE_DONE);
+  }
   MOE_TRY(launch_gemm(make_args(desc->bits, h, dt, w->w2, E, F, d, desc->group, offs, p.R, MOE_ACT_NONE,
                                     nullptr, MOE_F32, y), p.fc2, st));
   MOE_TRY(mark(MOE_STAGE_FC2));

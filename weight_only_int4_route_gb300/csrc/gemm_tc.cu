@@ -85,6 +85,8 @@ struct TcParams {
   const uint16_t *scales;
   void *out;
   int R, E, K, N, group, act, out_dtype, ncb, swiglu;
+  const int32_t *row_dest;   // fused top-1 un-permute (see GemmArgs), or nullptr
+  const float *row_gate;
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -271,6 +273,19 @@ __device__ __forceinline__ void epilogue_cols(const TcParams &p, const Tile &t, 
           if (j < nvalid) o[int64_t(j) * Nout] = from_f32<OT>(act_silu(v[j] * sc) * xbuf[j * 64 + r]);
       }
       asm volatile("bar.sync %0, 128;\n" ::"r"(bar_id) : "memory");
+    } else if (p.row_dest) {   // top-1 un-permute: row j goes to its token's row, times its gate
+      int dl = 0;
+      float gl = 0.f;
+      if (lane < nvalid) {
+        dl = p.row_dest[t.row0 + c0 + lane];
+        gl = p.row_gate[dl];
+      }
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int dj = __shfl_sync(0xffffffffu, dl, j);
+        const float gj = __shfl_sync(0xffffffffu, gl, j);
+        if (j < nvalid) static_cast<OT *>(p.out)[int64_t(dj) * Nout + ch] = from_f32<OT>((v[j] * sc) * gj);
+      }
     } else {
       OT *o = static_cast<OT *>(p.out) + int64_t(t.row0 + c0) * Nout + ch;
       if (p.act == MOE_ACT_GELU) {
@@ -636,6 +651,8 @@ int launch_typed(const GemmArgs &g, cudaStream_t st) {
     if (r != CUDA_SUCCESS) return set_error(MOE_ERR_CUDA, "weight tensor map encode failed (%d)", int(r));
   }
   TcParams tp{};
+  tp.row_dest = g.row_dest;
+  tp.row_gate = g.row_gate;
   tp.offsets = g.offsets;
   tp.scales = static_cast<const uint16_t *>(g.scales);
   tp.out = g.out;

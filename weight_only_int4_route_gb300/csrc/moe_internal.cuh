@@ -75,6 +75,10 @@ struct GemmArgs {
   int out_dtype;
   int a_dtype;
   int bits;
+  // tcgen05 kernel only, top-1 un-permute fused into the epilogue: permuted row p is written to
+  // output row row_dest[p], times row_gate[row_dest[p]] (nullptr: row p, no factor)
+  const int32_t *row_dest;
+  const float *row_gate;
 };
 // Enqueue the grouped GEMM described by `g` with plan `pl`.  When pl.partial, the fp32
 // accumulators (times per-channel scales) go to g.partial (splits, R, N).  Dispatches to the
