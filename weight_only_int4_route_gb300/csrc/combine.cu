@@ -196,6 +196,118 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(
   }
 }
 
+// Few output groups and many split slices (decode steps): summing the slices one after another
+// in each thread is a chain of dependent memory round trips.  Instead a CTA owns one (row,
+// 128-column group); its 8 warps each sum an interleaved subset of the (entry, slice) terms
+// (lane l: columns 4l .. 4l+3) and warp 0 adds the 8 partial sums in warp order.  The order is
+// fixed, so results are deterministic (it is a different order from the one-thread kernels).
+constexpr int kSmallWarps = 8;
+
+// out[r, c] = act(sum_s part[s, r, c]) (SWIGLU pairs c with c + N/2); Nout % 4 == 0.
+__global__ void __launch_bounds__(kSmallWarps * 32) reduce_act_small_kernel(const float *__restrict__ part, int splits,
+                                                                           int64_t R, int N, int act,
+                                                                           void *__restrict__ out, int out_dtype) {
+  __shared__ float4 red[2][kSmallWarps][32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool swiglu = act == MOE_ACT_SWIGLU;
+  const int Nout = swiglu ? N / 2 : N;
+  const int ngroups = (Nout + 127) / 128;
+  const int64_t r = blockIdx.x / ngroups;
+  const int c = (blockIdx.x % ngroups) * 128 + lane * 4;
+  const bool in = c < Nout;
+  float4 v = make_float4(0.f, 0.f, 0.f, 0.f), u = v;
+  if (in) {
+    const int64_t slice = R * int64_t(N);
+    const float *pv = part + r * N + c;
+    for (int s = warp; s < splits; s += kSmallWarps) {
+      const float4 q = *reinterpret_cast<const float4 *>(pv + s * slice);
+      v.x += q.x; v.y += q.y; v.z += q.z; v.w += q.w;
+      if (swiglu) {
+        const float4 w = *reinterpret_cast<const float4 *>(pv + s * slice + Nout);
+        u.x += w.x; u.y += w.y; u.z += w.z; u.w += w.w;
+      }
+    }
+  }
+  red[0][warp][lane] = v;
+  red[1][warp][lane] = u;
+  __syncthreads();
+  if (warp == 0 && in) {
+    float a[4] = {0.f, 0.f, 0.f, 0.f}, b[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int w = 0; w < kSmallWarps; ++w) {
+      const float4 x = red[0][w][lane], y = red[1][w][lane];
+      a[0] += x.x; a[1] += x.y; a[2] += x.z; a[3] += x.w;
+      b[0] += y.x; b[1] += y.y; b[2] += y.z; b[3] += y.w;
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float o = swiglu ? act_silu(a[q]) * b[q] : act_apply(a[q], act);
+      st_any(out, out_dtype, r * Nout + c + q, o);
+    }
+  }
+}
+
+// out[t] = sum_j gate[t, j] * sum_s y[s, inv[t*k + j]] + sum_s sh[s, t] for one (token,
+// 128-column group) per CTA; k <= 32 (lane j holds entry j).  Term q < k*ysplits is entry
+// q / ysplits, slice q % ysplits; the rest are shared-expert slices.
+__global__ void __launch_bounds__(kSmallWarps * 32) combine_small_kernel(
+    const void *__restrict__ y, int y_dtype, int ysplits, const int32_t *__restrict__ inv_perm,
+    const float *__restrict__ gate, const void *__restrict__ sh, int sh_dtype, int shsplits, int64_t T,
+    int64_t d, int k, void *__restrict__ out, int out_dtype) {
+  __shared__ float4 red[kSmallWarps][32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t R = T * k;
+  const int64_t ngroups = (d + 127) / 128;
+  const int64_t tok = blockIdx.x / ngroups;
+  const int64_t c = (blockIdx.x % ngroups) * 128 + lane * 4;
+  const bool in = c < d;
+  int pl = -1;
+  float gl = 0.f;
+  if (lane < k) {
+    pl = inv_perm[tok * k + lane];
+    gl = gate[tok * k + lane];
+    if (pl < 0 || pl >= R) pl = -1;   // malformed permutation: contributes nothing
+  }
+  const int ny = k * ysplits;
+  const int nterms = ny + (sh ? shsplits : 0);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int q = warp; q < nterms; q += kSmallWarps) {   // warp-uniform
+    if (q < ny) {
+      const int j = q / ysplits, s = q - j * ysplits;
+      const int p = __shfl_sync(0xffffffffu, pl, j);
+      const float g = __shfl_sync(0xffffffffu, gl, j);
+      if (p >= 0 && in) {
+        const float4 v = ld4(y, y_dtype, (int64_t(s) * R + p) * d + c);
+        acc.x += g * v.x; acc.y += g * v.y; acc.z += g * v.z; acc.w += g * v.w;
+      }
+    } else if (in) {
+      const float4 v = ld4(sh, sh_dtype, (int64_t(q - ny) * T + tok) * d + c);
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+  }
+  red[warp][lane] = acc;
+  __syncthreads();
+  if (warp == 0 && in) {
+    float a[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int w = 0; w < kSmallWarps; ++w) {
+      const float4 x = red[w][lane];
+      a[0] += x.x; a[1] += x.y; a[2] += x.z; a[3] += x.w;
+    }
+    if (out_dtype == MOE_F32) {
+      *reinterpret_cast<float4 *>(static_cast<float *>(out) + tok * d + c) = make_float4(a[0], a[1], a[2], a[3]);
+    } else {
+      uint2 v;
+      if (out_dtype == MOE_F16) {
+        v.x = h2_as_u32(__floats2half2_rn(a[0], a[1]));
+        v.y = h2_as_u32(__floats2half2_rn(a[2], a[3]));
+      } else {
+        v.x = h2_as_u32(__floats2bfloat162_rn(a[0], a[1]));
+        v.y = h2_as_u32(__floats2bfloat162_rn(a[2], a[3]));
+      }
+      *reinterpret_cast<uint2 *>(static_cast<char *>(out) + (tok * d + c) * 2) = v;
+    }
+  }
+}
+
 int grid_1d(int64_t total, int threads) {
   const int64_t want = cdiv(total, threads);
   const int64_t cap = int64_t(num_sms()) * 8;
@@ -208,7 +320,11 @@ int launch_reduce_act(const float *part, int splits, int64_t R, int N, int act, 
                       int out_dtype, cudaStream_t st) {
   const int Nout = act == MOE_ACT_SWIGLU ? N / 2 : N;
   if (R == 0) return MOE_OK;
-  reduce_act_kernel<<<grid_1d(R * Nout, 256), 256, 0, st>>>(part, splits, R, N, act, out, out_dtype);
+  const int64_t groups = R * cdiv(Nout, 128);
+  if (splits >= 4 && Nout % 4 == 0 && groups <= int64_t(num_sms()) * 4)   // few outputs, many slices
+    reduce_act_small_kernel<<<unsigned(groups), kSmallWarps * 32, 0, st>>>(part, splits, R, N, act, out, out_dtype);
+  else
+    reduce_act_kernel<<<grid_1d(R * Nout, 256), 256, 0, st>>>(part, splits, R, N, act, out, out_dtype);
   return check_launch("reduce_act");
 }
 
@@ -216,6 +332,12 @@ int launch_combine(const void *y, int y_dtype, int ysplits, const int32_t *inv_p
                    const float *gate, const void *sh, int sh_dtype, int shsplits, int64_t T,
                    int64_t d, int k, void *out, int out_dtype, cudaStream_t st) {
   if (T == 0) return MOE_OK;
+  const int64_t ngroups = T * cdiv(d, 128);
+  if (k <= 32 && k * ysplits + (sh ? shsplits : 0) >= 8 && ngroups <= int64_t(num_sms()) * 4) {
+    combine_small_kernel<<<unsigned(ngroups), kSmallWarps * 32, 0, st>>>(y, y_dtype, ysplits, inv_perm, gate, sh,
+                                                                         sh_dtype, shsplits, T, d, k, out, out_dtype);
+    return check_launch("combine");
+  }
   // two tokens x four 128-column strides per warp when that still leaves 16 work items per SM,
   // else one token x one stride (parallelism across columns for a few tokens)
   const int64_t g1 = T * cdiv(d, 128);

@@ -281,6 +281,36 @@ __global__ void __launch_bounds__(kThreads) route_reduce_topk_kernel(const float
   topk_softmax_warp(lg[warp], E, k, renorm, ids + int64_t(tok) * k, gates + int64_t(tok) * k);
 }
 
+// Few tokens, many K splits (decode): one CTA per token; warp w sums the slices s = w, w+8, ...
+// for every expert, warp 0 adds the 8 partial sums in warp order (+ bias), then top-k.  The order
+// is fixed (deterministic), different from the one-warp kernel's.
+__global__ void __launch_bounds__(kThreads * 2) route_reduce_small_kernel(const float *__restrict__ part, int S,
+                                                                        int T_, int E, const float *__restrict__ bias,
+                                                                        int k, int renorm, int32_t *__restrict__ ids,
+                                                                        float *__restrict__ gates) {
+  constexpr int kW = kThreads * 2 / 32;
+  __shared__ float red[kW][kMaxE];
+  __shared__ float lg[kMaxE];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int tok = blockIdx.x;
+  const int64_t sstride = int64_t(T_) * E;
+  for (int e = lane; e < E; e += 32) {
+    float v = 0.f;
+    for (int s = warp; s < S; s += kW) v += part[s * sstride + int64_t(tok) * E + e];
+    red[warp][e] = v;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    for (int e = lane; e < E; e += 32) {
+      float v = 0.f;
+      for (int w = 0; w < kW; ++w) v += red[w][e];
+      lg[e] = v + (bias ? bias[e] : 0.f);
+    }
+    __syncwarp();
+    topk_softmax_warp(lg, E, k, renorm, ids + int64_t(tok) * k, gates + int64_t(tok) * k);
+  }
+}
+
 int route_splits(int64_t T, int64_t d) {
   const int64_t ntt = cdiv(T, kPTok);
   const int64_t nkc = cdiv(d, kPKC);
@@ -345,8 +375,12 @@ extern "C" int moe_route_topk(const void *x, int x_dtype, const void *w_router, 
       else route_partial_kernel<__nv_bfloat16, 64><<<pgrid, kThreads, 0, st>>>(xb, wb, int(T), int(d), int(E), KS, part);
     }
     MOE_TRY(check_launch("route_partial"));
-    route_reduce_topk_kernel<<<unsigned(cdiv(T, kThreads / 32)), kThreads, 0, st>>>(part, S, int(T), int(E), bias, k,
-                                                                                 renormalize, ids, gate_w);
+    if (S >= 8 && T <= int64_t(num_sms()) * 2)
+      route_reduce_small_kernel<<<unsigned(T), kThreads * 2, 0, st>>>(part, S, int(T), int(E), bias, k, renormalize,
+                                                                       ids, gate_w);
+    else
+      route_reduce_topk_kernel<<<unsigned(cdiv(T, kThreads / 32)), kThreads, 0, st>>>(part, S, int(T), int(E), bias, k,
+                                                                                   renormalize, ids, gate_w);
   }
   return check_launch("route_topk");
 }
