@@ -33,6 +33,7 @@ from weight_only_int4_route_gb300 import synth  # noqa: E402
 
 METRIC = "MoE-layer tokens/s at 1 GB300; % of HBM (decode) / tensor (prefill) roofline"
 L2_BYTES = 129 * 1024 * 1024
+GRAPH_MAX_T = 32   # steps of at most this many tokens replay each layer's chain as a CUDA graph
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -48,6 +49,7 @@ def parse():
     ap.add_argument("--cpu-sample", type=int, default=256, help="tokens in the oracle's timed sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="decode-sized steps: launch kernels one by one")
     return ap.parse_args()
 
 
@@ -201,10 +203,24 @@ def run_ours(args, cfg, T, n_layers, world, rank, local):
     ws_bytes = M.Layer(packed[0], T).ws_bytes
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     layers = [M.Layer(p, T, workspace=ws) for p in packed]
+    # decode-sized steps run each layer's chain as one CUDA graph (fixed buffers, input resident)
+    use_graph = T <= GRAPH_MAX_T and not args.no_graph
+    graphs = []
+    if use_graph:
+        for li, layer in enumerate(layers):
+            g = M.LayerGraph(layer, T)
+            g.x.copy_(xs[0] if n_layers > 1 else xs[li % nx])
+            graphs.append(g)
     torch.cuda.synchronize()
 
     def step(i):
-        if n_layers > 1:
+        if use_graph:
+            if n_layers > 1:
+                for g in graphs:
+                    g.launch()
+            else:
+                graphs[i % copies].launch()
+        elif n_layers > 1:
             for li, layer in enumerate(layers):
                 layer.forward(xs[0], outs[li])
         else:
@@ -265,6 +281,17 @@ def run_ours(args, cfg, T, n_layers, world, rank, local):
         ksteps = max(3, min(args.steps, 50))
 
         def e2e_step(i):
+            if use_graph:   # the step's input goes into the graphs' input buffers
+                if n_layers > 1:
+                    for g in graphs:
+                        g.x.copy_(xh, non_blocking=True)
+                        g.launch()
+                    oh.copy_(graphs[-1].out, non_blocking=True)
+                else:
+                    g = graphs[i % copies]
+                    g.x.copy_(xh, non_blocking=True)
+                    oh.copy_(g.launch(), non_blocking=True)
+                return
             xd.copy_(xh, non_blocking=True)
             if n_layers > 1:
                 for li, layer in enumerate(layers):
@@ -307,7 +334,10 @@ def run_ours(args, cfg, T, n_layers, world, rank, local):
     ms = max_over_ranks(elapsed_ms / args.steps, dist, dev)
     if e2e is not None:
         e2e["ms"] = max_over_ranks(e2e["ms"], dist, dev)
+    for g in graphs:
+        g.close()
     return dict(ms=ms, stage_ms=stage_ms, counts=counts, clocks=clk, e2e=e2e, copies=copies,
+                launch="one CUDA graph per layer chain" if use_graph else "kernels launched one by one",
                 launches=launches_per_layer * n_layers * args.steps, per_layer_bytes=per_layer, kernels=kernels,
                 est_touch=est_touch, dist=dist)
 
@@ -418,7 +448,7 @@ def main():
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": r["ms"], "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
-            "config": dict(base_cfg, l2=(f"inputs larger than L2: {r['copies']} rotating weight/activation copies"
+            "config": dict(base_cfg, launch=r["launch"], l2=(f"inputs larger than L2: {r['copies']} rotating weight/activation copies"
                                          if n_layers == 1 else f"{n_layers} distinct layers per step"),
                            active_experts=wm["active_experts"],
                            layer_roofline={"hbm_frac": lw["bytes"] / (layer_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],

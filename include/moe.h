@@ -289,6 +289,26 @@ int moe_layer_forward_profiled(const moe_layer_desc *desc, const moe_layer_weigh
                                size_t workspace_bytes, moe_stream_t stream,
                                void *const *stage_events);
 
+/* ---- The layer chain as one CUDA graph (decode steps) ---------------------------------------
+ * A decode step runs the whole chain on a few tokens, where each kernel is short and the chain's
+ * cost is launch and dependency latency ("Specter", technical novelty: one launch for all expert
+ * sub-computations of a draft step).  moe_layer_graph_create runs moe_layer_forward once on
+ * `stream` (this also fills per-kernel caches that must not change during capture), then captures
+ * a second call into a CUDA graph and instantiates it.  The graph is bound to the pointers given:
+ * x, out, workspace and the weights must stay allocated and at the same addresses while the
+ * graph exists; the caller changes the input by writing into x.  T is fixed.  The caller owns
+ * the handle and releases it with moe_layer_graph_destroy.  `stream` must not be capturing
+ * already.  Errors: the moe_layer_forward checks, MOE_ERR_CUDA if capture or instantiation
+ * fails (no graph is returned then). */
+typedef struct moe_layer_graph_s *moe_layer_graph;
+int moe_layer_graph_create(const moe_layer_desc *desc, const moe_layer_weights *w, const void *x,
+                           int64_t T, void *out, void *workspace, size_t workspace_bytes,
+                           moe_stream_t stream, moe_layer_graph *graph);
+/* One replay of the captured chain on `stream` (asynchronous). */
+int moe_layer_graph_launch(moe_layer_graph graph, moe_stream_t stream);
+/* Frees the graph (NULL is a no-op).  No replay may be pending. */
+int moe_layer_graph_destroy(moe_layer_graph graph);
+
 #ifdef __cplusplus
 }
 #endif

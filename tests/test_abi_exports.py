@@ -65,6 +65,13 @@ def test_invalid_arguments_are_rejected_on_host(L):
     # misaligned pointer
     bad = ctypes.c_void_p(0x1003)
     assert L.moe_unpermute_combine(bad, 2, bad, bad, nul, 2, 4, 64, 1, bad, 0, nul) == -1
+    # layer graph: no handle pointer, T == 0, the legacy default stream; NULL destroy is a no-op
+    assert L.moe_layer_graph_create(None, None, nul, 4, nul, nul, 0, nul, None) == -1
+    h = ctypes.c_void_p()
+    assert L.moe_layer_graph_create(None, None, nul, 0, nul, nul, 0, nul, ctypes.byref(h)) == -1 and not h.value
+    assert L.moe_layer_graph_create(None, None, nul, 4, nul, nul, 0, nul, ctypes.byref(h)) == -1 and not h.value
+    assert L.moe_layer_graph_launch(nul, nul) == -1
+    assert L.moe_layer_graph_destroy(nul) == 0
 
 
 def test_layer_workspace_query(L):

@@ -433,3 +433,24 @@ def test_fused_top1_combine_is_bit_identical(M, name):
 def PackedLayer_from(cfg, w):
     from weight_only_int4_route_gb300.moe import PackedLayer
     return PackedLayer.from_weights(cfg, w, DEV)
+
+
+
+@pytest.mark.parametrize("name,T", [("qwen", 8), ("phi", 1), ("encdec_int4", 40)])
+def test_layer_graph_matches_forward(M, name, T):
+    """The chain captured as one CUDA graph gives the eager forward's output bit for bit, also
+    after a new input is written into the graph's input buffer."""
+    from weight_only_int4_route_gb300.moe import Layer, LayerGraph, PackedLayer
+    cfg = synth.CONFIGS[name]
+    w, x = layer_inputs(cfg, T)
+    layer = Layer(PackedLayer.from_weights(cfg, w, DEV), T)
+    g = LayerGraph(layer, T)
+    for rep in range(2):
+        xi = x if rep == 0 else synth.normal(cfg, "x", (T, cfg.d), 1.0, cfg.torch_dtype, extra=99)
+        g.x.copy_(xi.to(DEV))
+        got = g.launch().clone()
+        ref = layer.forward(xi.to(DEV))
+        torch.cuda.synchronize()
+        assert torch.equal(got, ref)
+    assert M.device_error(DEV) == 0
+    g.close()

@@ -388,3 +388,58 @@ extern "C" int moe_layer_forward_profiled(const moe_layer_desc *desc, const moe_
   MOE_TRY(launch_combine(y, MOE_F32, p.fc2.splits, inv, gate, sh, MOE_F32, shs, T, d, k, out, dt, st));
   return mark(MOE_STAGE_DONE);
 }
+
+// ---------------------------------------------------------------- CUDA graph of the chain
+
+struct moe_layer_graph_s {
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+};
+
+extern "C" int moe_layer_graph_create(const moe_layer_desc *desc, const moe_layer_weights *w, const void *x,
+                                      int64_t T, void *out, void *workspace, size_t workspace_bytes,
+                                      moe_stream_t stream, moe_layer_graph *graph) {
+  MOE_REQUIRE(graph != nullptr, "graph handle pointer is NULL");
+  *graph = nullptr;
+  MOE_REQUIRE(T > 0, "a graph needs T > 0");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  MOE_REQUIRE(st != nullptr, "capture needs a created stream (not the legacy default stream)");
+  // eager run: validates the arguments and fills the per-kernel caches before capture
+  MOE_TRY(moe_layer_forward(desc, w, x, T, out, workspace, workspace_bytes, stream));
+  if (cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal) != cudaSuccess)
+    return check_launch("layer graph: begin capture");
+  const int rc = moe_layer_forward(desc, w, x, T, out, workspace, workspace_bytes, stream);
+  cudaGraph_t g = nullptr;
+  const cudaError_t ec = cudaStreamEndCapture(st, &g);
+  if (rc != MOE_OK || ec != cudaSuccess || g == nullptr) {
+    if (g) cudaGraphDestroy(g);
+    cudaGetLastError();
+    return rc != MOE_OK ? rc : set_error(MOE_ERR_CUDA, "layer graph: capture failed: %s", cudaGetErrorString(ec));
+  }
+  cudaGraphExec_t ex = nullptr;
+  const cudaError_t ei = cudaGraphInstantiate(&ex, g, 0);
+  if (ei != cudaSuccess) {
+    cudaGraphDestroy(g);
+    return set_error(MOE_ERR_CUDA, "layer graph: instantiate failed: %s", cudaGetErrorString(ei));
+  }
+  auto *h = new moe_layer_graph_s;
+  h->graph = g;
+  h->exec = ex;
+  *graph = h;
+  return MOE_OK;
+}
+
+extern "C" int moe_layer_graph_launch(moe_layer_graph graph, moe_stream_t stream) {
+  MOE_REQUIRE(graph != nullptr && graph->exec != nullptr, "graph is NULL");
+  if (cudaGraphLaunch(graph->exec, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return check_launch("layer graph launch");
+  return MOE_OK;
+}
+
+extern "C" int moe_layer_graph_destroy(moe_layer_graph graph) {
+  if (graph == nullptr) return MOE_OK;
+  if (graph->exec) cudaGraphExecDestroy(graph->exec);
+  if (graph->graph) cudaGraphDestroy(graph->graph);
+  delete graph;
+  return MOE_OK;
+}

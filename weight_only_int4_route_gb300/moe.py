@@ -73,6 +73,10 @@ _SIGS = {
     "moe_layer_routing_view": (_c_int, [ctypes.POINTER(LayerDesc), _c_i64, _vp, ctypes.POINTER(LayerRouting)]),
     "moe_layer_launch_count": (_c_int, [ctypes.POINTER(LayerDesc), _c_i64]),
     "moe_layer_forward": (_c_int, [ctypes.POINTER(LayerDesc), ctypes.POINTER(LayerWeightsC), _vp, _c_i64, _vp, _vp, _c_size, _vp]),
+    "moe_layer_graph_create": (_c_int, [ctypes.POINTER(LayerDesc), ctypes.POINTER(LayerWeightsC), _vp, _c_i64, _vp,
+                                        _vp, ctypes.c_size_t, _vp, ctypes.POINTER(_vp)]),
+    "moe_layer_graph_launch": (_c_int, [_vp, _vp]),
+    "moe_layer_graph_destroy": (_c_int, [_vp]),
     "moe_layer_forward_profiled": (_c_int, [ctypes.POINTER(LayerDesc), ctypes.POINTER(LayerWeightsC), _vp, _c_i64, _vp, _vp,
                                             _c_size, _vp, ctypes.POINTER(_vp)]),
 }
@@ -336,3 +340,40 @@ class Layer:
         return dict(ids=view(v.ids, T * k, torch.int32).view(T, k), gate=view(v.gate_w, T * k, torch.float32).view(T, k),
                     offsets=view(v.offsets, E + 1, torch.int32), perm=view(v.perm, T * k, torch.int32),
                     inv_perm=view(v.inv_perm, T * k, torch.int32))
+
+
+class LayerGraph:
+    """A Layer's whole chain for a fixed T captured into one CUDA graph (moe_layer_graph_*).
+
+    The graph reads `self.x` and writes `self.out` (device buffers owned here): copy the step's
+    input into `x`, call `launch()`, read `out`."""
+
+    def __init__(self, layer: "Layer", T: int):
+        assert 0 < T <= layer.max_T
+        dev = layer.p.w1.device
+        self.layer, self.T = layer, T
+        self.x = torch.zeros((T, layer.cfg.d), dtype=layer.cfg.torch_dtype, device=dev)
+        self.out = torch.empty((T, layer.cfg.d), dtype=layer.cfg.torch_dtype, device=dev)
+        self.handle = _vp()
+        side = torch.cuda.Stream(device=dev)            # capture needs a created stream
+        side.wait_stream(torch.cuda.current_stream(dev))
+        _check(lib().moe_layer_graph_create(ctypes.byref(layer.desc), ctypes.byref(layer.wc), _ptr(self.x), T,
+                                            _ptr(self.out), _ptr(layer.ws), layer.ws.numel(),
+                                            ctypes.c_void_p(side.cuda_stream), ctypes.byref(self.handle)),
+               "moe_layer_graph_create")
+        torch.cuda.current_stream(dev).wait_stream(side)
+
+    def launch(self) -> torch.Tensor:
+        _check(lib().moe_layer_graph_launch(self.handle, _stream(self.x.device)), "moe_layer_graph_launch")
+        return self.out
+
+    def close(self):
+        if self.handle:
+            lib().moe_layer_graph_destroy(self.handle)
+            self.handle = _vp()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
