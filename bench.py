@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="decode-sized steps: launch kernels one by one")
+    ap.add_argument("--codec", action="store_true",
+                    help="time the BF16 bit-field recombine kernel instead of the layer (separate metric)")
     return ap.parse_args()
 
 
@@ -378,6 +380,52 @@ def cpu_baseline(cfg, T, sample, n_layers, min_seconds=10.0, max_rounds=200):
             "seconds": dt}
 
 
+def run_codec(args, world, rank, local):
+    """BF16 bit-field recombine (exponent bytes + sign|mantissa bytes -> BF16): an HBM stream of
+    4 bytes per element; 256 M elements per launch (1 GB moved, far above L2)."""
+    from weight_only_int4_route_gb300 import build as B
+    from weight_only_int4_route_gb300 import moe as M
+    B.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    n = 256 << 20
+    g = torch.Generator(device=dev).manual_seed(5)
+    w = (torch.randn(n, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+    exp, sm = M.bf16_split(w)
+    out = torch.empty_like(w)
+    del w
+    lib = M.lib()
+    st = M._stream(dev)
+
+    def step():
+        M._check(lib.moe_bf16_recombine(M._ptr(exp), M._ptr(sm), n, M._ptr(out), st), "moe_bf16_recombine")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        step()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    if M.device_error(dev):
+        raise SystemExit("bench: device error word set during the run; no result reported")
+    peaks, src = load_peaks()
+    gbs = 4.0 * n / (ms * 1e-3) / 1e9
+    line = {"metric": "BF16 bit-field recombine bandwidth (exponent + sign|mantissa bytes -> BF16)", "value": gbs,
+            "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+            "config": {"workload": f"{n} BF16 elements (N(0, 0.02) weights), 1 GB moved per launch"},
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"], "traffic": None, "peak_source": f"{src} HBM copy bandwidth",
+                         "kernel": "recombine_kernel", "algorithmic_bytes": 4 * n},
+            "gpu_launches": args.steps}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     world, rank, local = dist_env()
@@ -419,6 +467,8 @@ def main():
         print(json.dumps(line), flush=True)
         return
 
+    if args.codec:
+        return run_codec(args, world, rank, local)
     r = run_ours(args, cfg, T, n_layers, world, rank, local)
     peaks, peak_src = load_peaks()
     wm = work_model(cfg, T, r["counts"])

@@ -289,6 +289,15 @@ int moe_layer_forward_profiled(const moe_layer_desc *desc, const moe_layer_weigh
                                size_t workspace_bytes, moe_stream_t stream,
                                void *const *stage_events);
 
+/* ---- Lossless BF16 bit-field codec ("ZipMoE" summary page, method details) ------------------
+ * A BF16 expert tensor is stored as two byte planes: exp[i] = bits 14..7 of element i (the
+ * low-entropy part the host compresses), sm[i] = sign (bit 7) | mantissa (bits 6..0).
+ * moe_bf16_recombine merges the planes back into BF16 bit patterns, bit for bit;
+ * moe_bf16_split is its inverse.  n elements; all pointers device, 16-byte aligned; n may be
+ * any size (the last n % 16 elements take a scalar path).  Errors: MOE_ERR_INVALID_ARG. */
+int moe_bf16_recombine(const uint8_t *exp, const uint8_t *sm, int64_t n, uint16_t *out, moe_stream_t stream);
+int moe_bf16_split(const uint16_t *in, int64_t n, uint8_t *exp, uint8_t *sm, moe_stream_t stream);
+
 /* ---- The layer chain as one CUDA graph (decode steps) ---------------------------------------
  * A decode step runs the whole chain on a few tokens, where each kernel is short and the chain's
  * cost is launch and dependency latency ("Specter", technical novelty: one launch for all expert

@@ -72,6 +72,10 @@ def test_invalid_arguments_are_rejected_on_host(L):
     assert L.moe_layer_graph_create(None, None, nul, 4, nul, nul, 0, nul, ctypes.byref(h)) == -1 and not h.value
     assert L.moe_layer_graph_launch(nul, nul) == -1
     assert L.moe_layer_graph_destroy(nul) == 0
+    # bit-field codec: negative n, misaligned planes; n == 0 is a no-op
+    assert L.moe_bf16_recombine(nul, nul, -1, nul, nul) == -1
+    assert L.moe_bf16_recombine(bad, bad, 64, bad, nul) == -1
+    assert L.moe_bf16_split(nul, 0, nul, nul, nul) == 0
 
 
 def test_layer_workspace_query(L):

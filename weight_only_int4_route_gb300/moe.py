@@ -73,6 +73,8 @@ _SIGS = {
     "moe_layer_routing_view": (_c_int, [ctypes.POINTER(LayerDesc), _c_i64, _vp, ctypes.POINTER(LayerRouting)]),
     "moe_layer_launch_count": (_c_int, [ctypes.POINTER(LayerDesc), _c_i64]),
     "moe_layer_forward": (_c_int, [ctypes.POINTER(LayerDesc), ctypes.POINTER(LayerWeightsC), _vp, _c_i64, _vp, _vp, _c_size, _vp]),
+    "moe_bf16_recombine": (_c_int, [_vp, _vp, _c_i64, _vp, _vp]),
+    "moe_bf16_split": (_c_int, [_vp, _c_i64, _vp, _vp, _vp]),
     "moe_layer_graph_create": (_c_int, [ctypes.POINTER(LayerDesc), ctypes.POINTER(LayerWeightsC), _vp, _c_i64, _vp,
                                         _vp, ctypes.c_size_t, _vp, ctypes.POINTER(_vp)]),
     "moe_layer_graph_launch": (_c_int, [_vp, _vp]),
@@ -377,3 +379,22 @@ class LayerGraph:
             self.close()
         except Exception:
             pass
+
+
+def bf16_split(t: torch.Tensor):
+    """BF16 tensor -> (exponent bytes, sign|mantissa bytes), uint8 of t.numel() each."""
+    assert t.dtype == torch.bfloat16 and t.is_contiguous()
+    n = t.numel()
+    exp = torch.empty(n, dtype=torch.uint8, device=t.device)
+    sm = torch.empty(n, dtype=torch.uint8, device=t.device)
+    _check(lib().moe_bf16_split(_ptr(t), n, _ptr(exp), _ptr(sm), _stream(t.device)), "moe_bf16_split")
+    return exp, sm
+
+
+def bf16_recombine(exp: torch.Tensor, sm: torch.Tensor) -> torch.Tensor:
+    """(exponent bytes, sign|mantissa bytes) -> BF16 tensor of the same length."""
+    assert exp.dtype == sm.dtype == torch.uint8 and exp.numel() == sm.numel()
+    out = torch.empty(exp.numel(), dtype=torch.bfloat16, device=exp.device)
+    _check(lib().moe_bf16_recombine(_ptr(exp), _ptr(sm), exp.numel(), _ptr(out), _stream(exp.device)),
+           "moe_bf16_recombine")
+    return out
