@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="decode-sized steps: launch kernels one by one")
+    ap.add_argument("--elb", action="store_true",
+                    help="time ELB counting + top-M for one chunk boundary instead of the layer (separate metric)")
     ap.add_argument("--codec", action="store_true",
                     help="time the BF16 bit-field recombine kernel instead of the layer (separate metric)")
     return ap.parse_args()
@@ -380,6 +382,55 @@ def cpu_baseline(cfg, T, sample, n_layers, min_seconds=10.0, max_rounds=200):
             "seconds": dt}
 
 
+def run_elb(args, world, rank, local):
+    """Specter's expert lookahead buffer at one chunk boundary: accumulate the routed ids of a
+    32-step draft window for every MoE layer of a Qwen-shaped stack (24 layers, E=60, top-4),
+    then take each layer's top-8 experts.  Latency-bound (a few KB), so the metric is time."""
+    from weight_only_int4_route_gb300 import build as B
+    from weight_only_int4_route_gb300 import moe as M
+    B.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    L, S, k, E, Mtop = 24, 32, 4, 60, 8
+    g = torch.Generator(device=dev).manual_seed(9)
+    ids = torch.argsort(torch.rand((L, S, E), generator=g, device=dev), dim=-1)[..., :k].to(torch.int32).contiguous()
+    counts = torch.zeros((L, E), dtype=torch.int32, device=dev)
+    experts = torch.empty((L, Mtop), dtype=torch.int32, device=dev)
+    vals = torch.empty((L, Mtop), dtype=torch.int32, device=dev)
+    lib, st = M.lib(), M._stream(dev)
+    args_c = (M._ptr(ids), L, S, k, E, M._ptr(counts), Mtop, M._ptr(experts), M._ptr(vals), st)
+
+    def step():   # one launch through the C ABI: accumulate + top-M
+        M._check(lib.moe_elb_step(*args_c), "moe_elb_step")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        step()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    if M.device_error(dev):
+        raise SystemExit("bench: device error word set during the run; no result reported")
+    peaks, src = load_peaks()
+    nbytes = ids.numel() * 4 + 3 * counts.numel() * 4 + 2 * L * Mtop * 4
+    line = {"metric": "ELB boundary latency (accumulate a 32-step draft window for 24 layers + top-8 per layer)",
+            "value": ms * 1e3, "unit": "us", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "int32",
+            "data": "synthetic", "config": {"workload": f"L={L} layers, S={S} draft steps, top-{k} of E={E}, M={Mtop}"},
+            "roofline": {"bound": "hbm", "achieved": nbytes / (ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], "traffic": None,
+                         "peak_source": f"{src} HBM copy bandwidth", "kernel": "elb_step_kernel",
+                         "algorithmic_bytes": nbytes,
+                         "note": "a few KB per boundary: the launch's latency, not bandwidth, is the cost"},
+            "gpu_launches": args.steps}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def run_codec(args, world, rank, local):
     """BF16 bit-field recombine (exponent bytes + sign|mantissa bytes -> BF16): an HBM stream of
     4 bytes per element; 256 M elements per launch (1 GB moved, far above L2)."""
@@ -469,6 +520,8 @@ def main():
 
     if args.codec:
         return run_codec(args, world, rank, local)
+    if args.elb:
+        return run_elb(args, world, rank, local)
     r = run_ours(args, cfg, T, n_layers, world, rank, local)
     peaks, peak_src = load_peaks()
     wm = work_model(cfg, T, r["counts"])

@@ -298,6 +298,23 @@ int moe_layer_forward_profiled(const moe_layer_desc *desc, const moe_layer_weigh
 int moe_bf16_recombine(const uint8_t *exp, const uint8_t *sm, int64_t n, uint16_t *out, moe_stream_t stream);
 int moe_bf16_split(const uint16_t *in, int64_t n, uint8_t *exp, uint8_t *sm, moe_stream_t stream);
 
+/* ---- Expert lookahead buffer ("Specter" summary page, method steps (2)-(3)) -----------------
+ * moe_elb_accumulate: counts (L, E) int32, row-major, += for every layer j and expert e the
+ * number of draft steps i < S with e among ids[j, i, 0..k-1] (ids (L, S, k) int32: the routed
+ * ids of S draft steps; an expert counts once per step, ids outside [0, E) are skipped).
+ * moe_elb_topm: for every layer, the min(M, E) experts with the largest counts, by count
+ * descending then expert id ascending -> experts (L, min(M, E)) and their counts vals (same
+ * shape).  Integer results, independent of launch configuration.  Device pointers; errors:
+ * MOE_ERR_INVALID_ARG (E > 256, k > 64, L > 65535, NULL). */
+int moe_elb_accumulate(const int32_t *ids, int64_t L, int64_t S, int k, int64_t E, int32_t *counts,
+                       moe_stream_t stream);
+int moe_elb_topm(const int32_t *counts, int64_t L, int64_t E, int M, int32_t *experts, int32_t *vals,
+                 moe_stream_t stream);
+/* Both in one launch: accumulate the window's ids into counts, then write every layer's top-M of
+ * the updated counts (same results as moe_elb_accumulate followed by moe_elb_topm). */
+int moe_elb_step(const int32_t *ids, int64_t L, int64_t S, int k, int64_t E, int32_t *counts, int M,
+                 int32_t *experts, int32_t *vals, moe_stream_t stream);
+
 /* ---- The layer chain as one CUDA graph (decode steps) ---------------------------------------
  * A decode step runs the whole chain on a few tokens, where each kernel is short and the chain's
  * cost is launch and dependency latency ("Specter", technical novelty: one launch for all expert

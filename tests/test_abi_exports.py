@@ -76,6 +76,10 @@ def test_invalid_arguments_are_rejected_on_host(L):
     assert L.moe_bf16_recombine(nul, nul, -1, nul, nul) == -1
     assert L.moe_bf16_recombine(bad, bad, 64, bad, nul) == -1
     assert L.moe_bf16_split(nul, 0, nul, nul, nul) == 0
+    # ELB: E above 256, k out of range; L == 0 is a no-op
+    assert L.moe_elb_accumulate(nul, 2, 4, 2, 300, nul, nul) == -1
+    assert L.moe_elb_accumulate(nul, 2, 4, 0, 8, nul, nul) == -1
+    assert L.moe_elb_topm(nul, 0, 8, 2, nul, nul, nul) == 0
 
 
 def test_layer_workspace_query(L):

@@ -75,6 +75,9 @@ _SIGS = {
     "moe_layer_forward": (_c_int, [ctypes.POINTER(LayerDesc), ctypes.POINTER(LayerWeightsC), _vp, _c_i64, _vp, _vp, _c_size, _vp]),
     "moe_bf16_recombine": (_c_int, [_vp, _vp, _c_i64, _vp, _vp]),
     "moe_bf16_split": (_c_int, [_vp, _c_i64, _vp, _vp, _vp]),
+    "moe_elb_accumulate": (_c_int, [_vp, _c_i64, _c_i64, _c_int, _c_i64, _vp, _vp]),
+    "moe_elb_topm": (_c_int, [_vp, _c_i64, _c_i64, _c_int, _vp, _vp, _vp]),
+    "moe_elb_step": (_c_int, [_vp, _c_i64, _c_i64, _c_int, _c_i64, _vp, _c_int, _vp, _vp, _vp]),
     "moe_layer_graph_create": (_c_int, [ctypes.POINTER(LayerDesc), ctypes.POINTER(LayerWeightsC), _vp, _c_i64, _vp,
                                         _vp, ctypes.c_size_t, _vp, ctypes.POINTER(_vp)]),
     "moe_layer_graph_launch": (_c_int, [_vp, _vp]),
@@ -398,3 +401,29 @@ def bf16_recombine(exp: torch.Tensor, sm: torch.Tensor) -> torch.Tensor:
     _check(lib().moe_bf16_recombine(_ptr(exp), _ptr(sm), exp.numel(), _ptr(out), _stream(exp.device)),
            "moe_bf16_recombine")
     return out
+
+
+def elb_accumulate(ids: torch.Tensor, E: int, counts: torch.Tensor) -> torch.Tensor:
+    """ids (L, S, k) int32 draft-step routes; counts (L, E) int32, updated in place."""
+    L, S, k = ids.shape
+    assert ids.dtype == counts.dtype == torch.int32 and counts.shape == (L, E)
+    _check(lib().moe_elb_accumulate(_ptr(ids), L, S, k, E, _ptr(counts), _stream(ids.device)), "moe_elb_accumulate")
+    return counts
+
+
+def elb_topm(counts: torch.Tensor, M: int):
+    """counts (L, E) int32 -> (experts, counts) of each layer's top-M, (L, min(M, E)) int32."""
+    L, E = counts.shape
+    m = min(M, E)
+    ex = torch.empty((L, m), dtype=torch.int32, device=counts.device)
+    vals = torch.empty((L, m), dtype=torch.int32, device=counts.device)
+    _check(lib().moe_elb_topm(_ptr(counts), L, E, M, _ptr(ex), _ptr(vals), _stream(counts.device)), "moe_elb_topm")
+    return ex, vals
+
+
+def elb_step(ids: torch.Tensor, E: int, counts: torch.Tensor, M: int, experts: torch.Tensor, vals: torch.Tensor):
+    """elb_accumulate followed by elb_topm in one launch, into preallocated (L, min(M, E)) outputs."""
+    L, S, k = ids.shape
+    _check(lib().moe_elb_step(_ptr(ids), L, S, k, E, _ptr(counts), M, _ptr(experts), _ptr(vals), _stream(ids.device)),
+           "moe_elb_step")
+    return experts, vals
