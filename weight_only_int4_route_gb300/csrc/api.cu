@@ -164,6 +164,41 @@ LayerPlan plan_layer(const moe_layer_desc *d, int64_t T) {
   return p;
 }
 
+// The shared expert reads only x, so it runs on a second stream beside the routed chain
+// (router, sort, two grouped GEMMs) and joins back before the combine: its 16-bit weight stream
+// overlaps the chain's short, latency-bound kernels.  One stream and two events per thread and
+// device, made on first use and kept for the life of the process (a graph capture records the
+// fork and the join as graph edges).
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+int side_stream(SideStream **out) {
+  thread_local SideStream tl[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return check_launch("side stream: cudaGetDevice");
+  if (dev < 0 || dev >= 64) return set_error(MOE_ERR_UNSUPPORTED, "side stream: device index %d >= 64", dev);
+  SideStream &sd = tl[dev];
+  if (sd.s == nullptr) {
+    cudaStream_t s = nullptr;
+    cudaEvent_t f = nullptr, j = nullptr;
+    if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&f, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&j, cudaEventDisableTiming) != cudaSuccess) {
+      if (j) cudaEventDestroy(j);
+      if (f) cudaEventDestroy(f);
+      if (s) cudaStreamDestroy(s);
+      return check_launch("side stream: create");
+    }
+    sd.s = s;
+    sd.fork = f;
+    sd.join = j;
+  }
+  *out = &sd;
+  return MOE_OK;
+}
+
 GemmArgs make_args(int bits, const void *a, int dt, const void *w, int64_t E, int64_t K, int64_t N,
                    int group, const int32_t *offsets, int64_t R, int act, void *out, int out_dtype,
                    float *partial) {
@@ -345,10 +380,32 @@ extern "C" int moe_layer_forward_profiled(const moe_layer_desc *desc, const moe_
       return check_launch("stage event");
     return MOE_OK;
   };
+  // shared expert beside the routed chain (serial when stage events are recorded, so that every
+  // stage boundary stays a point in one stream)
+  SideStream *side = nullptr;
+  if (desc->Fs > 0 && !stage_events) {
+    MOE_TRY(side_stream(&side));
+    if (cudaEventRecord(side->fork, st) != cudaSuccess) return check_launch("shared expert: fork");
+  }
+  auto shared_expert = [&](cudaStream_t s) -> int {
+    void *hs = ws + p.o_hs;
+    float *ps1 = reinterpret_cast<float *>(ws + p.o_ps1);
+    float *ys = reinterpret_cast<float *>(ws + p.o_ys);
+    MOE_TRY(launch_gemm(make_args(16, x, dt, w->ws_gate_up, 1, d, 2 * desc->Fs, 0, nullptr, T,
+                                  MOE_ACT_SWIGLU, hs, dt, ps1), p.sh1, s));
+    if (p.sh1.partial) MOE_TRY(launch_reduce_act(ps1, p.sh1.splits, T, int(2 * desc->Fs), MOE_ACT_SWIGLU, hs, dt, s));
+    return launch_gemm(make_args(16, hs, dt, w->ws_down, 1, desc->Fs, d, 0, nullptr, T, MOE_ACT_NONE, nullptr,
+                                 MOE_F32, ys), p.sh2, s);
+  };
   MOE_TRY(mark(MOE_STAGE_START));
   MOE_TRY(moe_route_topk(x, dt, w->w_router, desc->router_dtype, w->router_bias, T, d, E, k,
                          desc->renormalize, ids, gate, ws + p.o_rws, moe_route_topk_workspace_size(T, d, E),
                          stream));
+  if (side) {   // enqueued after the router, so the router's blocks are placed first
+    if (cudaStreamWaitEvent(side->s, side->fork, 0) != cudaSuccess) return check_launch("shared expert: wait");
+    MOE_TRY(shared_expert(side->s));
+    if (cudaEventRecord(side->join, side->s) != cudaSuccess) return check_launch("shared expert: join");
+  }
   MOE_TRY(mark(MOE_STAGE_ROUTED));
   MOE_TRY(moe_permute(ids, x, dt, T, d, E, k, offs, perm, inv, xp, ws + p.o_pws,
                       moe_permute_workspace_size(T, E, k), stream));
@@ -373,15 +430,12 @@ extern "C" int moe_layer_forward_profiled(const moe_layer_desc *desc, const moe_
   const void *sh = nullptr;
   int shs = 0;
   if (desc->Fs > 0) {
-    void *hs = ws + p.o_hs;
-    float *ps1 = reinterpret_cast<float *>(ws + p.o_ps1);
-    float *ys = reinterpret_cast<float *>(ws + p.o_ys);
-    MOE_TRY(launch_gemm(make_args(16, x, dt, w->ws_gate_up, 1, d, 2 * desc->Fs, 0, nullptr, T,
-                                      MOE_ACT_SWIGLU, hs, dt, ps1), p.sh1, st));
-    if (p.sh1.partial) MOE_TRY(launch_reduce_act(ps1, p.sh1.splits, T, int(2 * desc->Fs), MOE_ACT_SWIGLU, hs, dt, st));
-    MOE_TRY(launch_gemm(make_args(16, hs, dt, w->ws_down, 1, desc->Fs, d, 0, nullptr, T, MOE_ACT_NONE,
-                                      nullptr, MOE_F32, ys), p.sh2, st));
-    sh = ys;
+    if (side) {
+      if (cudaStreamWaitEvent(st, side->join, 0) != cudaSuccess) return check_launch("shared expert: join wait");
+    } else {
+      MOE_TRY(shared_expert(st));
+    }
+    sh = ws + p.o_ys;
     shs = p.sh2.splits;
   }
   MOE_TRY(mark(MOE_STAGE_SHARED));

@@ -40,14 +40,14 @@ constexpr int kMaxE = 256;
 template <int BITS, int NT, int MT> struct GV {
   static constexpr int kVec = BITS / 4;                      // 16-byte pieces per channel per lane
   static constexpr int kRows = 16 * MT;                      // weight rows per unit
-  static constexpr int kLanesPerRow = 32 / kRows;            // lanes that copy one row
   static constexpr int kRowBytes = 16 * BITS;                // bytes of one row per chunk
   static constexpr int kRowStride = kRowBytes + (BITS == 4 ? 0 : 16);
-  // INT4 rows are 64 bytes: piece p of row r sits at p ^ ((r / 2) % 4), so the lanes' copies
-  // (one row each) and reads (two rows per 8 lanes) both spread over all banks
-  static constexpr bool kSwizzle = BITS == 4;
-  __host__ __device__ static constexpr int piece_at(int r, int p) { return kSwizzle ? (p ^ ((r >> 1) & 3)) : p; }
-  static constexpr int kWPieces = kRowBytes / 16 / kLanesPerRow;   // pieces a lane copies
+  // A quarter-warp reads the same pieces of two adjacent rows: 64-byte INT4 rows put them on
+  // different banks as they are, the 16 bytes of padding do it for 8- and 16-bit rows.  Copies
+  // write whole rows, kRowsPerCopy of them per warp-wide copy.
+  static constexpr int kWPieces = kRows * kRowBytes / 16 / 32;   // pieces a lane copies per chunk
+  static constexpr int kPiecesPerRow = kRowBytes / 16;
+  static constexpr int kRowsPerCopy = 32 / kPiecesPerRow;          // rows one warp-wide copy covers
   static constexpr int kXOff = kRows * kRowStride;
   static constexpr int kSOff = kXOff + NT * 4 * 512;
   static constexpr int kScaleLanes = MT * 2;                 // 16-byte scale pieces per chunk
@@ -204,8 +204,8 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GvParams p) {
   const int F = p.N >> 1;
   const uint32_t wring = smem_u32(gv_ring) + warp * C::kWarpBytes;
   const unsigned char *rring = gv_ring + warp * C::kWarpBytes;   // the same ring, for reads
-  // this lane's weight reads: row g (+ 8 h + 16 m, whose swizzle equals row g's), pieces from t * kVec
-  const uint32_t wlane = g * C::kRowStride + C::piece_at(g, t * kVec) * 16;
+  // this lane's weight reads: row g (+ 8 h + 16 m), pieces from t * kVec
+  const uint32_t wlane = g * C::kRowStride + t * kVec * 16;
 
   // output channel of m-tile m, A row r (0..15), channel group grp
   auto channel = [&](int grp, int m, int r) -> int {
@@ -213,11 +213,13 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GvParams p) {
     return (grp * MT + m) * 16 + r;
   };
 
-  // ---- copy side.  Lane i copies C::kWPieces pieces of weight row i / kLanesPerRow, its own
+  // ---- copy side.  Copy v of a step moves C::kRowsPerCopy whole weight rows (consecutive lanes
+  // take consecutive 16-byte pieces of a row, so every request fills whole sectors); lane i takes
+  // piece i % kPiecesPerRow of row v * kRowsPerCopy + i / kPiecesPerRow.  Each lane also copies its own
   // activation pieces (row g of each n-tile, reduction indices [32t, 32t+32)), and lanes below
   // kScaleLanes one 16-byte piece of the scale rows.
-  const int wrow = lane / C::kLanesPerRow;
-  const int wpart = lane % C::kLanesPerRow;
+  const int wrow = lane / C::kPiecesPerRow;   // row of copy 0; copy v adds v * kRowsPerCopy
+  const int wpart = lane % C::kPiecesPerRow;
   Stride dstep;
   Cursor icur, ccur;   // issue side and compute side
   {
@@ -231,15 +233,20 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GvParams p) {
     ccur = icur;
   }
   int iu = 0, ic = 0;
-  const uint4 *wsrc = nullptr;
+  const uint4 *wbase = nullptr;   // the unit's expert and K range; rows at woff[v] pieces from it
+  int woff[C::kWPieces];
   const uint4 *ssrc = nullptr;
   const uint4 *xsrc[NT];
   int xbytes[NT];
   auto load_unit = [&]() {
     const Unit x = unit_of<NT>(icur, s_rcstart, s_off);
     const int kc0 = x.s * p.CH;
-    const int ch = channel(x.grp, wrow / 16, wrow % 16);
-    wsrc = p.w + (int64_t(x.e) * p.N + ch) * w_row_vec + int64_t(kc0) * BITS + wpart * C::kWPieces;
+    wbase = p.w + int64_t(x.e) * p.N * w_row_vec + int64_t(kc0) * BITS + wpart;
+#pragma unroll
+    for (int v = 0; v < C::kWPieces; ++v) {
+      const int r = v * C::kRowsPerCopy + wrow;
+      woff[v] = channel(x.grp, r / 16, r % 16) * int(w_row_vec);
+    }
     if (grouped && lane < C::kScaleLanes) {   // piece q: the 8 channels of A rows 8 (q % 2) .. of m-tile q / 2
       const int c0 = channel(x.grp, lane >> 1, 8 * (lane & 1));
       ssrc = reinterpret_cast<const uint4 *>(p.scales + (int64_t(x.e) * G + kc0) * p.N + c0);
@@ -254,10 +261,11 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GvParams p) {
   };
   auto issue = [&](int slot) {
     const uint32_t sb = wring + slot * C::kSlotBytes;
-    const uint4 *ws = wsrc + ic * BITS;
 #pragma unroll
-    for (int v = 0; v < C::kWPieces; ++v)
-      cp_w16(sb + wrow * C::kRowStride + C::piece_at(wrow, wpart * C::kWPieces + v) * 16, ws + v);
+    for (int v = 0; v < C::kWPieces; ++v) {
+      const int r = v * C::kRowsPerCopy + wrow;
+      cp_w16(sb + r * C::kRowStride + wpart * 16, wbase + (woff[v] + ic * BITS));
+    }
 #pragma unroll
     for (int n = 0; n < NT; ++n)
 #pragma unroll
@@ -475,8 +483,9 @@ int blocks_per_sm(bool bf, int bits, int nt, int mt, bool grouped) {
 
 bool gemv_shape_ok(int64_t K, int64_t N, int bits, int act) {
   const int64_t m16 = act == MOE_ACT_SWIGLU ? (N / 2) / 8 : N / 16;   // 16-channel m-tiles
+  // one expert's rows are addressed by 32-bit offsets in 16-byte pieces
   return K % 128 == 0 && (act == MOE_ACT_SWIGLU ? (N / 2) % 8 == 0 : N % 16 == 0) &&
-         (bits == 16 || m16 % 2 == 0);
+         (bits == 16 || m16 % 2 == 0) && N * (K * bits / 128) < (int64_t(1) << 31);
 }
 
 // Plan for the decode kernel.  The routing is not known on the host, so the number of row
