@@ -454,3 +454,25 @@ def test_layer_graph_matches_forward(M, name, T):
         assert torch.equal(got, ref)
     assert M.device_error(DEV) == 0
     g.close()
+
+
+@pytest.mark.parametrize("name,T", [("qwen", 8), ("dsv2", 300)])
+def test_forked_shared_expert_matches_serial(M, name, T):
+    """With a shared expert, moe_layer_forward runs it on a second stream beside the routed
+    chain and joins before the combine; the profiled forward (stage events) runs the same
+    kernels in one stream.  Both give the same output bit for bit, over repeated calls."""
+    from weight_only_int4_route_gb300.moe import STAGES, Layer, PackedLayer
+    cfg = synth.CONFIGS[name]
+    assert cfg.Fs > 0
+    w, x = layer_inputs(cfg, T)
+    layer = Layer(PackedLayer.from_weights(cfg, w, DEV), T)
+    xd = x.to(DEV)
+    events = [torch.cuda.Event(enable_timing=True) for _ in STAGES]
+    for e in events:   # torch creates the CUDA event on its first record
+        e.record()
+    serial = layer.forward_profiled(xd, torch.empty((T, cfg.d), dtype=x.dtype, device=DEV), events).clone()
+    for _ in range(3):
+        forked = layer.forward(xd)
+        torch.cuda.synchronize()
+        assert torch.equal(forked, serial)
+    assert M.device_error(DEV) == 0
