@@ -476,3 +476,30 @@ def test_forked_shared_expert_matches_serial(M, name, T):
         torch.cuda.synchronize()
         assert torch.equal(forked, serial)
     assert M.device_error(DEV) == 0
+
+
+def test_gelu_same_bits_on_every_path(M):
+    """The tensor-memory GEMM evaluates GELU two at a time with paired fp32 instructions, the
+    decode GEMM one at a time; the operations and their order are the same, so the outputs are
+    the same bits (one weight of 1: every GEMM result is x itself)."""
+    E, K, N = 1, 128, 128
+
+    def run(x):
+        R = x.shape[0]
+        a = torch.zeros((R, K), dtype=torch.float16)
+        a[:, 0] = x
+        q = torch.zeros((E, K, N), dtype=torch.int8)
+        q[0, 0, :] = 1
+        s = torch.ones((E, 1, N), dtype=torch.float16)
+        packed = M.pack_weights(q.to(DEV), s.to(DEV), 4, 0)
+        off = torch.tensor([0, R], dtype=torch.int32)
+        out = M.grouped_gemm(a.to(DEV), packed, 4, E, K, N, 0, off.to(DEV), "gelu", torch.float32).cpu()
+        return out, M.gemm_path(R, E, K, N, 4, 0, "gelu")
+
+    x = torch.linspace(-9.0, 9.0, 1024).to(torch.float16)
+    tc, p_tc = run(x)
+    pick = torch.arange(0, 1024, 64)
+    gv, p_gv = run(x[pick])
+    assert (p_tc, p_gv) == ("tcgen05", "gemv")
+    assert M.device_error(DEV) == 0
+    assert torch.equal(tc[pick], gv)

@@ -290,8 +290,12 @@ __device__ __forceinline__ void epilogue_cols(const TcParams &p, const Tile &t, 
       OT *o = static_cast<OT *>(p.out) + int64_t(t.row0 + c0) * Nout + ch;
       if (p.act == MOE_ACT_GELU) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (j < nvalid) o[int64_t(j) * Nout] = from_f32<OT>(act_gelu(v[j] * sc));
+        for (int j = 0; j < 32; j += 2) {   // two GELUs per paired-fp32 evaluation
+          float g0 = v[j] * sc, g1 = v[j + 1] * sc;
+          act_gelu2(g0, g1);
+          if (j < nvalid) o[int64_t(j) * Nout] = from_f32<OT>(g0);
+          if (j + 1 < nvalid) o[int64_t(j + 1) * Nout] = from_f32<OT>(g1);
+        }
       } else if (p.act == MOE_ACT_RELU) {
 #pragma unroll
         for (int j = 0; j < 32; ++j)

@@ -219,7 +219,71 @@ __device__ __forceinline__ float act_gelu(float x) {
   const float q = 0.5f * x * P * e;
   return x >= 0.f ? x - q : q;
 }
-__device__ __forceinline__ float act_silu(float x) { return x / (1.0f + expf(-x)); }
+// Two GELUs with the same operations in the same order as act_gelu (so the same bits), the
+// fp32 arithmetic done by the paired .f32x2 instructions (two lanes of fp32 per instruction);
+// the reciprocal and the exponential stay per element.
+__device__ __forceinline__ void act_gelu2(float &x0, float &x1) {
+  float r0, r1;
+  asm("{\n"
+      " .reg .b64 x, z, d, t, P, a, e, q, h, c;\n"
+      " .reg .f32 z0, z1, d0, d1, t0, t1, a0, a1, e0, e1, r0, r1, q0, q1;\n"
+      " .reg .pred p0, p1;\n"
+      " mov.b64 x, {%2, %3};\n"
+      " mul.f32 z0, %2, 0f3F3504F3;\n"           // |x| / sqrt 2 (abs folded below)
+      " abs.f32 z0, z0;\n"
+      " mul.f32 z1, %3, 0f3F3504F3;\n"
+      " abs.f32 z1, z1;\n"
+      " mov.b64 z, {z0, z1};\n"
+      " mov.b64 c, {0f3EA7BA05, 0f3EA7BA05};\n"   // p = 0.3275911
+      " mov.b64 h, {0f3F800000, 0f3F800000};\n"
+      " fma.rn.f32x2 d, c, z, h;\n"
+      " mov.b64 {d0, d1}, d;\n"
+      " rcp.approx.ftz.f32 t0, d0;\n"
+      " rcp.approx.ftz.f32 t1, d1;\n"
+      " mov.b64 t, {t0, t1};\n"
+      " mov.b64 c, {0f3F87DC22, 0f3F87DC22};\n"   // a5 = 1.061405429
+      " mov.b64 h, {0fBFBA00E3, 0fBFBA00E3};\n"   // a4 = -1.453152027
+      " fma.rn.f32x2 P, c, t, h;\n"
+      " mov.b64 h, {0f3FB5F0E3, 0f3FB5F0E3};\n"   // a3 = 1.421413741
+      " fma.rn.f32x2 P, P, t, h;\n"
+      " mov.b64 h, {0fBE91A98E, 0fBE91A98E};\n"   // a2 = -0.284496736
+      " fma.rn.f32x2 P, P, t, h;\n"
+      " mov.b64 h, {0f3E827906, 0f3E827906};\n"   // a1 = 0.254829592
+      " fma.rn.f32x2 P, P, t, h;\n"
+      " mul.rn.f32x2 P, P, t;\n"
+      " mul.rn.f32x2 a, z, z;\n"
+      " mov.b64 c, {0fBFB8AA3B, 0fBFB8AA3B};\n"   // -log2(e)
+      " mul.rn.f32x2 a, a, c;\n"
+      " mov.b64 {a0, a1}, a;\n"
+      " ex2.approx.ftz.f32 e0, a0;\n"
+      " ex2.approx.ftz.f32 e1, a1;\n"
+      " mov.b64 e, {e0, e1};\n"
+      " mov.b64 c, {0f3F000000, 0f3F000000};\n"   // 0.5
+      " mul.rn.f32x2 q, c, x;\n"
+      " mul.rn.f32x2 q, q, P;\n"
+      " mul.rn.f32x2 q, q, e;\n"
+      " sub.rn.f32x2 d, x, q;\n"
+      " mov.b64 {d0, d1}, d;\n"
+      " mov.b64 {q0, q1}, q;\n"
+      " setp.ge.f32 p0, %2, 0f00000000;\n"
+      " setp.ge.f32 p1, %3, 0f00000000;\n"
+      " selp.f32 %0, d0, q0, p0;\n"
+      " selp.f32 %1, d1, q1, p1;\n"
+      "}\n"
+      : "=f"(r0), "=f"(r1)
+      : "f"(x0), "f"(x1));
+  x0 = r0;
+  x1 = r1;
+}
+// SiLU(x) = x / (1 + exp(-x)) with the hardware exponential and reciprocal approximations
+// (relative error a few 1e-7, far below the 16-bit rounding of every output it feeds); for very
+// negative x the exponential overflows to +inf and the result is -0, the limit.
+__device__ __forceinline__ float act_silu(float x) {
+  float e, r;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(e) : "f"(x * -1.4426950408889634f));
+  asm("rcp.approx.ftz.f32 %0, %1;\n" : "=f"(r) : "f"(1.0f + e));
+  return x * r;
+}
 __device__ __forceinline__ float act_apply(float x, int act) {
   return act == MOE_ACT_RELU ? act_relu(x) : (act == MOE_ACT_GELU ? act_gelu(x) : x);
 }
