@@ -503,3 +503,34 @@ def test_gelu_same_bits_on_every_path(M):
     assert (p_tc, p_gv) == ("tcgen05", "gemv")
     assert M.device_error(DEV) == 0
     assert torch.equal(tc[pick], gv)
+
+
+def test_silu_same_bits_on_every_path(M):
+    """SwiGLU through the tensor-memory GEMM (SiLU two at a time, paired fp32) and through the
+    decode GEMM (one at a time): gate = x, up = 1, so the output is SiLU(x) on both, bit for bit."""
+    E, K, N = 1, 128, 256
+    F = N // 2
+
+    def run(x):
+        R = x.shape[0]
+        a = torch.zeros((R, K), dtype=torch.bfloat16)
+        a[:, 0] = x
+        a[:, 1] = 1.0
+        q = torch.zeros((E, K, N), dtype=torch.int8)
+        q[0, 0, :F] = 1     # gate channels read x
+        q[0, 1, F:] = 1     # up channels read 1
+        s = torch.ones((E, K // 128, N), dtype=torch.bfloat16)
+        packed = M.pack_weights(q.to(DEV), s.to(DEV), 4, 128)
+        off = torch.tensor([0, R], dtype=torch.int32)
+        out = M.grouped_gemm(a.to(DEV), packed, 4, E, K, N, 128, off.to(DEV), "swiglu", torch.float32).cpu()
+        return out, M.gemm_path(R, E, K, N, 4, 128, "swiglu")
+
+    x = torch.linspace(-12.0, 12.0, 1024).to(torch.bfloat16)
+    tc, p_tc = run(x)
+    pick = torch.arange(0, 1024, 64)
+    gv, p_gv = run(x[pick])
+    assert (p_tc, p_gv) == ("tcgen05", "gemv")
+    assert M.device_error(DEV) == 0
+    assert torch.equal(tc[pick], gv)
+    ref = x.double() / (1.0 + torch.exp(-x.double()))
+    assert (tc.double() - ref[:, None]).abs().max().item() <= 1e-6 * max(1.0, ref.abs().max().item())

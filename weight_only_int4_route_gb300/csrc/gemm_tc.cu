@@ -269,8 +269,12 @@ __device__ __forceinline__ void epilogue_cols(const TcParams &p, const Tile &t, 
       if (q < 2) {
         OT *o = static_cast<OT *>(p.out) + int64_t(t.row0 + c0) * Nout + t.cb * (kBM / 2) + r;
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (j < nvalid) o[int64_t(j) * Nout] = from_f32<OT>(act_silu(v[j] * sc) * xbuf[j * 64 + r]);
+        for (int j = 0; j < 32; j += 2) {   // two SiLUs per paired-fp32 evaluation
+          float g0 = v[j] * sc, g1 = v[j + 1] * sc;
+          act_silu2(g0, g1);
+          if (j < nvalid) o[int64_t(j) * Nout] = from_f32<OT>(g0 * xbuf[j * 64 + r]);
+          if (j + 1 < nvalid) o[int64_t(j + 1) * Nout] = from_f32<OT>(g1 * xbuf[(j + 1) * 64 + r]);
+        }
       }
       asm volatile("bar.sync %0, 128;\n" ::"r"(bar_id) : "memory");
     } else if (p.row_dest) {   // top-1 un-permute: row j goes to its token's row, times its gate

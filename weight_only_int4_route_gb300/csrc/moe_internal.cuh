@@ -284,6 +284,33 @@ __device__ __forceinline__ float act_silu(float x) {
   asm("rcp.approx.ftz.f32 %0, %1;\n" : "=f"(r) : "f"(1.0f + e));
   return x * r;
 }
+// Two SiLUs, the same operations in the same order as act_silu, fp32 arithmetic paired.
+__device__ __forceinline__ void act_silu2(float &x0, float &x1) {
+  float r0, r1;
+  asm("{\n"
+      " .reg .b64 x, c, a, d, r;\n"
+      " .reg .f32 a0, a1, e0, e1, d0, d1, q0, q1;\n"
+      " mov.b64 x, {%2, %3};\n"
+      " mov.b64 c, {0fBFB8AA3B, 0fBFB8AA3B};\n"   // -log2(e)
+      " mul.rn.f32x2 a, x, c;\n"
+      " mov.b64 {a0, a1}, a;\n"
+      " ex2.approx.ftz.f32 e0, a0;\n"
+      " ex2.approx.ftz.f32 e1, a1;\n"
+      " mov.b64 d, {e0, e1};\n"
+      " mov.b64 c, {0f3F800000, 0f3F800000};\n"
+      " add.rn.f32x2 d, c, d;\n"
+      " mov.b64 {d0, d1}, d;\n"
+      " rcp.approx.ftz.f32 q0, d0;\n"
+      " rcp.approx.ftz.f32 q1, d1;\n"
+      " mov.b64 r, {q0, q1};\n"
+      " mul.rn.f32x2 r, x, r;\n"
+      " mov.b64 {%0, %1}, r;\n"
+      "}\n"
+      : "=f"(r0), "=f"(r1)
+      : "f"(x0), "f"(x1));
+  x0 = r0;
+  x1 = r1;
+}
 __device__ __forceinline__ float act_apply(float x, int act) {
   return act == MOE_ACT_RELU ? act_relu(x) : (act == MOE_ACT_GELU ? act_gelu(x) : x);
 }
