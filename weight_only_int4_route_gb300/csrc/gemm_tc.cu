@@ -9,22 +9,24 @@
 //   * A operand = dequantized weights, written by dequant warps straight into tensor memory
 //     (tcgen05.st), never through shared memory: shared-memory bandwidth is left to the
 //     activation operand.
-//   * B operand = 128 consecutive rows of the expert's segment of Xp, TMA-loaded with
+//   * B operand = up to 160 consecutive rows (128 for 16-bit weights) of the expert's segment of Xp, TMA-loaded with
 //     128-byte swizzle (K-major), so the MMA reads it through a shared-memory descriptor.
 //   * D = fp32 accumulator in tensor memory, double-buffered so the epilogue of one tile
 //     overlaps the mainloop of the next.
 //
 // Warp roles (one CTA per SM, persistent over tiles):
-//   warps 0-7    epilogue: warp w reads TMEM lanes 32*(w%4).. and one half of the tile's
-//                columns; scale / activation, global stores;
+//   warps 0-7    epilogue: warp w reads TMEM lanes 32*(w%4).. and every other 32-column chunk
+//                of the tile's columns; scale / activation, global stores;
 //   warp 8       producer: TMA of the packed weight block and the activation block;
 //   warp 9       MMA issuer (one thread);
-//   warps 10-17  dequant, two groups of four warps; group g converts the K blocks with
-//                index = g (mod 2), so each pipeline stage always belongs to the same group.  Warp w owns TMEM lanes 32*(w%4).. (one output channel
-//                per lane); it reads that channel's packed words from shared memory,
-//                converts them with the magic-number I2F (and the group-128 scale) and
-//                stores the 16-bit pairs into the A stage.
-// TMEM columns: [0,256) two 128-column accumulators, [256,512) four 64-column A stages.
+//   warps 10-21  dequant, three groups of four warps; group g converts the K blocks with
+//                index = g (mod 3), so each pipeline stage always belongs to the same group.
+//                Warp w owns TMEM lanes 32*(w%4).. (one output channel per lane); it reads
+//                that channel's packed words from shared memory, converts them with the
+//                magic-number I2F (and the group-128 scale) and stores the 16-bit pairs into
+//                the A stage.
+// Tiles are 128 output channels x up to 160 routed rows (an expert with up to 160 rows is one
+// tile).  TMEM columns: [0,320) two 160-column accumulators, [320,512) three 64-column A stages.
 //
 // Synchronisation per 128-wide K block: the producer's TMA completes `full`; the dequant
 // group waits on it, fills the TMEM A stage and arrives on `ready`; the MMA thread waits
@@ -48,24 +50,33 @@ __device__ int g_moe_device_error = 0;
 namespace {
 
 constexpr int kEpiWarps = 8;        // epilogue warps (two per TMEM lane quarter)
-constexpr int kDqGroups = 2;        // dequant warp groups (each: 4 warps covering 128 lanes)
+constexpr int kDqGroups = 3;        // dequant warp groups (each: 4 warps covering 128 lanes)
 constexpr int kProdWarp = kEpiWarps, kMmaWarp = kEpiWarps + 1, kDqWarp0 = kEpiWarps + 2;
 constexpr int kThreads = (kDqWarp0 + 4 * kDqGroups) * 32;
 constexpr int kBM = 128;          // output channels per tile (MMA M)
-constexpr int kBN = 128;          // rows per tile (MMA N upper bound)
+constexpr int kBNMax = 160;       // rows per tile at most (MMA N upper bound)
 constexpr int kBK = 128;          // K per pipeline stage
-constexpr int kStagesQ = 4;       // pipeline stages (shared memory and TMEM A), quantized weights
+constexpr int kStagesQ = 3;       // pipeline stages (shared memory and TMEM A), quantized weights
 // Every fill of a stage must go to the same dequant group.  A group waits on full[s] by phase
 // parity, which cannot tell "one phase ahead" from "complete": with groups taking K blocks
 // round-robin over a stage count they do not divide, the group of fill it + kStages could reach
 // full[s] while fill it (another group's) was still in flight -- TMA completions of different
 // stages are not ordered -- and pass the wait at once.
 static_assert(kStagesQ % kDqGroups == 0, "each stage must belong to one dequant group");
+static_assert(kBNMax % 32 == 0 && kBNMax <= 256, "tile rows: whole 32-column epilogue chunks, MMA N <= 256");
 constexpr int kMaxE = 256;
-constexpr int kBHalf = kBN * 64 * 2;         // one 64-wide swizzle atom column block: 16 KB
-constexpr int kBBytes = 2 * kBHalf;          // activation stage: 32 KB
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kACol0 = 256;
+// Tile geometry.  Quantized weights: up to 160 rows per tile, so an expert with up to 160 routed
+// rows is one tile (a second, nearly empty tile would repeat the whole dequant of its weights);
+// tensor memory holds two 160-column accumulators and three 64-column A stages.  16-bit weights
+// (A from shared memory, 32 KB per stage) keep 128 rows.
+template <int BITS> struct TB {
+  static constexpr int kBN = BITS == 16 ? 128 : kBNMax;   // rows per tile
+  static constexpr int kBHalf = kBN * 64 * 2;             // one 64-wide swizzle atom column block
+  static constexpr int kBBytes = 2 * kBHalf;              // activation stage
+  static constexpr uint32_t kACol0 = 2 * kBN;             // A stages after the two accumulators
+};
+static_assert(2 * kBNMax + kStagesQ * 64 <= 512, "tensor memory: accumulators + A stages");
 constexpr uint32_t kAStageCols = kBK / 2;    // 64 columns of 16-bit pairs
 constexpr long long kTimeoutCycles = 4000000000LL;  // ~2 s at 2 GHz
 
@@ -223,7 +234,8 @@ struct Tile {
   int e, row0, nrows, cb;
 };
 
-__device__ __forceinline__ Tile decode_tile(int tile, const int *s_tstart, const int *s_off, int E, int ncb) {
+__device__ __forceinline__ Tile decode_tile(int tile, const int *s_tstart, const int *s_off, int E, int ncb,
+                                            int bn) {
   int lo = 0, hi = E - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -235,8 +247,8 @@ __device__ __forceinline__ Tile decode_tile(int tile, const int *s_tstart, const
   const int in_e = tile - s_tstart[lo];
   const int tt = in_e / ncb;
   t.cb = in_e - tt * ncb;
-  t.row0 = s_off[lo] + tt * kBN;
-  t.nrows = min(kBN, s_off[lo + 1] - t.row0);
+  t.row0 = s_off[lo] + tt * bn;
+  t.nrows = min(bn, s_off[lo + 1] - t.row0);
   return t;
 }
 
@@ -249,14 +261,14 @@ template <typename OT> __device__ __forceinline__ void store_typed(void *out, in
 // the up quarters hand their values to the gate quarters through shared memory.
 template <typename T, typename OT>
 __device__ __forceinline__ void epilogue_cols(const TcParams &p, const Tile &t, uint32_t tmem_d, int q, int lane,
-                                              int c_lo, int c_hi, float *xbuf, int bar_id) {
+                                              int c_lo, int c_hi, int c_step, float *xbuf, int bar_id) {
   const int r = q * 32 + lane;
   int ch;
   if (p.swiglu) ch = r < kBM / 2 ? t.cb * (kBM / 2) + r : (p.N >> 1) + t.cb * (kBM / 2) + (r - kBM / 2);
   else ch = t.cb * kBM + r;
   const float sc = (p.group == 0 && p.scales) ? ldscale<T>(p.scales, int64_t(t.e) * p.N + ch) : 1.0f;
   const int Nout = p.swiglu ? (p.N >> 1) : p.N;
-  for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
+  for (int c0 = c_lo; c0 < c_hi; c0 += c_step) {
     float v[32];
     tc_ld32(tmem_d + (uint32_t(q * 32) << 16) + uint32_t(c0), v);
     const int nvalid = min(32, t.nrows - c0);
@@ -320,9 +332,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kWBytes = WB<BITS>::kBytes;
   constexpr int kWords = WB<BITS>::kWordsPerRow;
   constexpr int kStages = WB<BITS>::kStages;
+  constexpr int kBN = TB<BITS>::kBN, kBHalf = TB<BITS>::kBHalf, kBBytes = TB<BITS>::kBBytes;
+  constexpr uint32_t kACol0 = TB<BITS>::kACol0;
   extern __shared__ __align__(1024) uint8_t dsmem[];
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dsmem) + 1023) & ~uintptr_t(1023));
-  uint8_t *sB = base;                                   // kStages x 32 KB (two 1024-aligned 16 KB halves)
+  uint8_t *sB = base;                                   // kStages x kBBytes (two 1024-aligned K halves)
   uint8_t *sW = sB + kStages * kBBytes;                 // kStages x kWBytes
   float *sX = reinterpret_cast<float *>(sW + kStages * kWBytes);  // SwiGLU exchange: 2 halves x 32 x 64 fp32
   uint64_t *bar = reinterpret_cast<uint64_t *>(sX + 2 * 32 * 64);
@@ -382,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr int kPrefetch = 8;
       int pf_tile = blockIdx.x, pf_kb = 0, pf_A = 0, pf_B = 0;
       auto pf_rows = [&]() {
-        const Tile tn = decode_tile(pf_tile, s_tstart, s_off, E, p.ncb);
+        const Tile tn = decode_tile(pf_tile, s_tstart, s_off, E, p.ncb, kBN);
         pf_A = tn.e * p.N + (p.swiglu ? tn.cb * (kBM / 2) : tn.cb * kBM);
         pf_B = p.swiglu ? tn.e * p.N + (p.N >> 1) + tn.cb * (kBM / 2) : pf_A + kBM / 2;
       };
@@ -412,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < kStages; ++s) issued[s] = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-        const Tile t = decode_tile(tile, s_tstart, s_off, E, p.ncb);
+        const Tile t = decode_tile(tile, s_tstart, s_off, E, p.ncb, kBN);
         const int rowA = t.e * p.N + (p.swiglu ? t.cb * (kBM / 2) : t.cb * kBM);
         const int rowB = p.swiglu ? t.e * p.N + (p.N >> 1) + t.cb * (kBM / 2) : rowA + kBM / 2;
         for (int kb = 0; kb < nkb; ++kb, ++it) {
@@ -452,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t it = 0, tcount = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x, ++tcount) {
-        const Tile t = decode_tile(tile, s_tstart, s_off, E, p.ncb);
+        const Tile t = decode_tile(tile, s_tstart, s_off, E, p.ncb, kBN);
         const int n = (t.nrows + 15) & ~15;
         const uint32_t idesc = idesc_f16(is_bf16, kBM, n);
         const int db = tcount & 1;
@@ -497,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t it = 0;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-      const Tile t = decode_tile(tile, s_tstart, s_off, E, p.ncb);
+      const Tile t = decode_tile(tile, s_tstart, s_off, E, p.ncb, kBN);
       int ch;
       if (p.swiglu) ch = r < kBM / 2 ? t.cb * (kBM / 2) + r : (p.N >> 1) + t.cb * (kBM / 2) + (r - kBM / 2);
       else ch = t.cb * kBM + r;
@@ -567,20 +581,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------ epilogue (warps 0-7)
     const int q = warp & 3;
-    const int half = warp >> 2;   // tile columns [64*half, 64*half + 64)
+    const int half = warp >> 2;   // tile columns: 32-wide chunks 2 c + half
     uint32_t tcount = 0;
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++tcount) {
-      const Tile t = decode_tile(tile, s_tstart, s_off, E, p.ncb);
+      const Tile t = decode_tile(tile, s_tstart, s_off, E, p.ncb, kBN);
       const int db = tcount & 1;
       if (!mbar_wait(&d_full[db], (tcount >> 1) & 1, abort_flag, kErrTimeoutD)) break;
       tc_fence_after();
-      const int c_lo = 64 * half, c_hi = min(64 * half + 64, t.nrows);
+      const int c_lo = 32 * half, c_hi = t.nrows;
       const uint32_t tmem_d = tmem + uint32_t(db * kBN);
       float *xbuf = sX + half * (32 * 64);
       if (c_lo < c_hi) {
-        if (p.out_dtype == MOE_F32) epilogue_cols<T, float>(p, t, tmem_d, q, lane, c_lo, c_hi, xbuf, 1 + half);
-        else if (p.out_dtype == MOE_F16) epilogue_cols<T, __half>(p, t, tmem_d, q, lane, c_lo, c_hi, xbuf, 1 + half);
-        else epilogue_cols<T, __nv_bfloat16>(p, t, tmem_d, q, lane, c_lo, c_hi, xbuf, 1 + half);
+        if (p.out_dtype == MOE_F32) epilogue_cols<T, float>(p, t, tmem_d, q, lane, c_lo, c_hi, 64, xbuf, 1 + half);
+        else if (p.out_dtype == MOE_F16) epilogue_cols<T, __half>(p, t, tmem_d, q, lane, c_lo, c_hi, 64, xbuf, 1 + half);
+        else epilogue_cols<T, __nv_bfloat16>(p, t, tmem_d, q, lane, c_lo, c_hi, 64, xbuf, 1 + half);
       }
       tc_fence_before();
       __syncwarp();
@@ -619,7 +633,8 @@ EncodeTiledFn encode_fn() {
 size_t smem_bytes(int bits) {
   const size_t wbytes = bits == 4 ? WB<4>::kBytes : (bits == 8 ? WB<8>::kBytes : WB<16>::kBytes);
   const int st = bits == 16 ? WB<16>::kStages : kStagesQ;
-  return 1024 /*align slack*/ + st * (kBBytes + wbytes) + 2 * 32 * 64 * 4 + (3 * st + 5) * 8 +
+  const size_t bbytes = bits == 16 ? TB<16>::kBBytes : TB<4>::kBBytes;
+  return 1024 /*align slack*/ + st * (bbytes + wbytes) + 2 * 32 * 64 * 4 + (3 * st + 5) * 8 +
          (2 * (kMaxE + 1) + 32 + 2) * 4;
 }
 
@@ -631,7 +646,7 @@ int launch_typed(const GemmArgs &g, cudaStream_t st) {
   {
     const cuuint64_t dims[2] = {cuuint64_t(g.K), cuuint64_t(g.R)};
     const cuuint64_t strides[1] = {cuuint64_t(g.K) * 2};
-    const cuuint32_t box[2] = {64u, cuuint32_t(kBN)};  // one 128-byte swizzle atom column block
+    const cuuint32_t box[2] = {64u, cuuint32_t(TB<BITS>::kBN)};  // one 128-byte swizzle atom column block
     const cuuint32_t es[2] = {1, 1};
     const CUresult r = enc(&mx, std::is_same<T, __half>::value ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                            2, const_cast<void *>(g.a), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -683,7 +698,7 @@ int launch_typed(const GemmArgs &g, cudaStream_t st) {
     done = true;
   }
   // tiles upper bound: (row tiles) x channel blocks
-  const int64_t row_tiles = std::min<int64_t>(g.E, g.R) + cdiv(g.R, kBN);
+  const int64_t row_tiles = std::min<int64_t>(g.E, g.R) + cdiv(g.R, TB<BITS>::kBN);
   const int64_t tiles = row_tiles * tp.ncb;
   const int grid = int(std::max<int64_t>(1, std::min<int64_t>(tiles, num_sms())));
   gemm_tc_kernel<T, BITS><<<grid, kThreads, smem, st>>>(mx, mw, tp);
