@@ -18,6 +18,7 @@ __device__ __forceinline__ void st_any(void *p, int dt, int64_t i, float v) {
 // out[r, c] = act(sum_s part[s, r, c]); SWIGLU: silu(sum part[.., c]) * sum part[.., c + N/2].
 __global__ void reduce_act_kernel(const float *__restrict__ part, int splits, int64_t R, int N,
                                   int act, void *__restrict__ out, int out_dtype) {
+  pdl_enter();   // see launch_pdl
   const int Nout = act == MOE_ACT_SWIGLU ? N / 2 : N;
   const int64_t total = R * Nout;
   const int64_t slice = R * int64_t(N);
@@ -90,6 +91,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(
     const void *__restrict__ y, int y_dtype, int ysplits, const int32_t *__restrict__ inv_perm,
     const float *__restrict__ gate, const void *__restrict__ sh, int sh_dtype, int shsplits, int64_t T,
     int64_t d, int k, void *__restrict__ out, int out_dtype) {
+  pdl_enter();   // see launch_pdl
   const int lane = threadIdx.x & 31;
   const int64_t R = T * k;
   const int64_t ngroups = (d + 128 * CPT - 1) / (128 * CPT);
@@ -207,6 +209,7 @@ constexpr int kSmallWarps = 8;
 __global__ void __launch_bounds__(kSmallWarps * 32) reduce_act_small_kernel(const float *__restrict__ part, int splits,
                                                                            int64_t R, int N, int act,
                                                                            void *__restrict__ out, int out_dtype) {
+  pdl_enter();   // see launch_pdl
   __shared__ float4 red[2][kSmallWarps][32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool swiglu = act == MOE_ACT_SWIGLU;
@@ -253,6 +256,7 @@ __global__ void __launch_bounds__(kSmallWarps * 32) combine_small_kernel(
     const void *__restrict__ y, int y_dtype, int ysplits, const int32_t *__restrict__ inv_perm,
     const float *__restrict__ gate, const void *__restrict__ sh, int sh_dtype, int shsplits, int64_t T,
     int64_t d, int k, void *__restrict__ out, int out_dtype) {
+  pdl_enter();   // see launch_pdl
   __shared__ float4 red[kSmallWarps][32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t R = T * k;
@@ -322,9 +326,9 @@ int launch_reduce_act(const float *part, int splits, int64_t R, int N, int act, 
   if (R == 0) return MOE_OK;
   const int64_t groups = R * cdiv(Nout, 128);
   if (splits >= 4 && Nout % 4 == 0 && groups <= int64_t(num_sms()) * 4)   // few outputs, many slices
-    reduce_act_small_kernel<<<unsigned(groups), kSmallWarps * 32, 0, st>>>(part, splits, R, N, act, out, out_dtype);
+    launch_pdl(reduce_act_small_kernel, dim3(unsigned(groups)), dim3(kSmallWarps * 32), 0, st, part, splits, R, N, act, out, out_dtype);
   else
-    reduce_act_kernel<<<grid_1d(R * Nout, 256), 256, 0, st>>>(part, splits, R, N, act, out, out_dtype);
+    launch_pdl(reduce_act_kernel, dim3(grid_1d(R * Nout, 256)), dim3(256), 0, st, part, splits, R, N, act, out, out_dtype);
   return check_launch("reduce_act");
 }
 
@@ -334,7 +338,7 @@ int launch_combine(const void *y, int y_dtype, int ysplits, const int32_t *inv_p
   if (T == 0) return MOE_OK;
   const int64_t ngroups = T * cdiv(d, 128);
   if (k <= 32 && k * ysplits + (sh ? shsplits : 0) >= 8 && ngroups <= int64_t(num_sms()) * 4) {
-    combine_small_kernel<<<unsigned(ngroups), kSmallWarps * 32, 0, st>>>(y, y_dtype, ysplits, inv_perm, gate, sh,
+    launch_pdl(combine_small_kernel, dim3(unsigned(ngroups)), dim3(kSmallWarps * 32), 0, st, y, y_dtype, ysplits, inv_perm, gate, sh,
                                                                          sh_dtype, shsplits, T, d, k, out, out_dtype);
     return check_launch("combine");
   }
@@ -347,10 +351,10 @@ int launch_combine(const void *y, int y_dtype, int ysplits, const int32_t *inv_p
   const int64_t cap = int64_t(num_sms()) * 8;
   const unsigned grid = unsigned(want < cap ? want : cap);
   if (wide)
-    combine_kernel<4, 2><<<grid, kCombineWarps * 32, 0, st>>>(y, y_dtype, ysplits, inv_perm, gate, sh, sh_dtype,
+    launch_pdl(combine_kernel<4, 2>, dim3(grid), dim3(kCombineWarps * 32), 0, st, y, y_dtype, ysplits, inv_perm, gate, sh, sh_dtype,
                                                               shsplits, T, d, k, out, out_dtype);
   else
-    combine_kernel<1, 1><<<grid, kCombineWarps * 32, 0, st>>>(y, y_dtype, ysplits, inv_perm, gate, sh, sh_dtype,
+    launch_pdl(combine_kernel<1, 1>, dim3(grid), dim3(kCombineWarps * 32), 0, st, y, y_dtype, ysplits, inv_perm, gate, sh, sh_dtype,
                                                               shsplits, T, d, k, out, out_dtype);
   return check_launch("combine");
 }

@@ -120,6 +120,7 @@ __device__ __forceinline__ float ld_scale(const uint16_t *s, int64_t idx) {
 
 template <typename T, int BITS, int MB>
 __global__ void __launch_bounds__(kThreads) gemm_mma_kernel(const KParams p) {
+  pdl_enter();   // see launch_pdl
   constexpr int MT = 16 * MB;
   constexpr int kVec = WT<BITS>::kVec;
   constexpr int kPre = WT<BITS>::kPre;
@@ -312,7 +313,7 @@ int launch_one(const KParams &kp, int64_t items_upper, cudaStream_t st) {
   }
   const int64_t cap = int64_t(num_sms()) * occ[dev];
   const int grid = int(std::max<int64_t>(1, std::min<int64_t>(items_upper, cap)));
-  gemm_mma_kernel<T, BITS, MB><<<grid, kThreads, 0, st>>>(kp);
+  launch_pdl(gemm_mma_kernel<T, BITS, MB>, dim3(grid), dim3(kThreads), 0, st, kp);
   return check_launch("grouped_gemm");
 }
 

@@ -329,6 +329,7 @@ template <typename T, int BITS>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
                    const TcParams p) {
+  pdl_enter();   // see launch_pdl
   constexpr int kWBytes = WB<BITS>::kBytes;
   constexpr int kWords = WB<BITS>::kWordsPerRow;
   constexpr int kStages = WB<BITS>::kStages;
@@ -701,7 +702,7 @@ int launch_typed(const GemmArgs &g, cudaStream_t st) {
   const int64_t row_tiles = std::min<int64_t>(g.E, g.R) + cdiv(g.R, TB<BITS>::kBN);
   const int64_t tiles = row_tiles * tp.ncb;
   const int grid = int(std::max<int64_t>(1, std::min<int64_t>(tiles, num_sms())));
-  gemm_tc_kernel<T, BITS><<<grid, kThreads, smem, st>>>(mx, mw, tp);
+  launch_pdl(gemm_tc_kernel<T, BITS>, dim3(grid), dim3(kThreads), smem, st, mx, mw, tp);
   return check_launch("grouped_gemm_tc");
 }
 

@@ -162,6 +162,7 @@ __device__ __forceinline__ Unit unit_of(const Cursor &c, const int *s_rcstart, c
 // per-channel scales (applied at the end) or none (16-bit weights).
 template <typename T, int BITS, int NT, int MT, bool GROUPED>
 __global__ void __launch_bounds__(kThreads) gemv_kernel(const GvParams p) {
+  pdl_enter();   // see launch_pdl
   using C = GV<BITS, NT, MT>;
   constexpr int kVec = C::kVec, kDepth = C::kDepth;
   extern __shared__ __align__(128) unsigned char gv_ring[];
@@ -561,6 +562,8 @@ int launch_gemv(const GemmArgs &g, const GemmPlan &pl, cudaStream_t st) {
                      static_cast<long long>(units_max));
   const int64_t resident = int64_t(num_sms()) * blocks_per_sm(bf, g.bits, pl.nt, pl.mt, grouped);
   const int grid = int(std::max<int64_t>(1, std::min<int64_t>(resident, cdiv(units_max, kWarps))));
+  // a plain launch: placed early, its blocks (all of the SMs' shared memory) would wait there and
+  // keep a concurrent branch (the shared expert's stream) off the SMs
   in.fn<<<grid, kThreads, in.smem, st>>>(gp);
   return check_launch("grouped_gemv");
 }

@@ -16,6 +16,28 @@ int set_error(int code, const char *fmt, ...);
 int check_launch(const char *what);  // MOE_OK or MOE_ERR_CUDA with the runtime's message
 int num_sms();                       // SM count of the current device (cached)
 
+// Programmatic dependent launch.  The kernels of the layer chain are launched with programmatic
+// stream serialization: a kernel may be placed on the SMs while its predecessor in the stream is
+// still running, and its first act (pdl_enter) is to let its own successor be launched likewise
+// and then wait until the predecessor has completed and its memory is visible -- before any
+// global memory is read or written, so the stream order of every access is as without it.  A
+// kernel launched without the attribute passes the wait at once.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 inline bool is16(int dt) { return dt == MOE_F16 || dt == MOE_BF16; }
@@ -313,6 +335,11 @@ __device__ __forceinline__ void act_silu2(float &x0, float &x1) {
 }
 __device__ __forceinline__ float act_apply(float x, int act) {
   return act == MOE_ACT_RELU ? act_relu(x) : (act == MOE_ACT_GELU ? act_gelu(x) : x);
+}
+
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
 }
 
 // ---- warp-level tensor-core MMA (m16n8k16, fp32 accumulate) ---------------------------

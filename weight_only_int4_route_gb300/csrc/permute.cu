@@ -27,6 +27,7 @@ constexpr int kFusedScanMax = 16384;   // tile-count entries up to which the sca
 
 __global__ void __launch_bounds__(kTile) count_kernel(const int32_t *__restrict__ ids, int64_t R,
                                                       int E, int32_t *__restrict__ tile_counts) {
+  pdl_enter();   // see launch_pdl
   __shared__ int cnt[kMaxE];
   for (int e = threadIdx.x; e < E; e += kTile) cnt[e] = 0;
   __syncthreads();
@@ -44,6 +45,7 @@ __global__ void __launch_bounds__(kTile) count_kernel(const int32_t *__restrict_
 __global__ void __launch_bounds__(kMaxE) scan_kernel(const int32_t *__restrict__ tile_counts,
                                                      int ntiles, int E, int32_t *__restrict__ tile_base,
                                                      int32_t *__restrict__ offsets) {
+  pdl_enter();   // see launch_pdl
   __shared__ int scratch[32];
   const int e = threadIdx.x;
   int total = 0;
@@ -117,6 +119,7 @@ __global__ void __launch_bounds__(kTile) scatter_kernel(const int32_t *__restric
                                                         int32_t *__restrict__ perm,
                                                         int32_t *__restrict__ inv_perm,
                                                         uint8_t *__restrict__ xp) {
+  pdl_enter();   // see launch_pdl
   __shared__ int wcount[kTile / 32][kMaxE];
   __shared__ int dest[kTile];
   __shared__ int tot[kMaxE], pre[kMaxE];
@@ -186,6 +189,7 @@ __global__ void __launch_bounds__(kSmall) permute_small_kernel(const int32_t *__
                                                                int32_t *__restrict__ perm,
                                                                int32_t *__restrict__ inv_perm,
                                                                uint8_t *__restrict__ xp) {
+  pdl_enter();   // see launch_pdl
   __shared__ int wcount[kSmall / 32][kMaxE];
   __shared__ int s_off[kMaxE];
   __shared__ int dest[kSmall];
@@ -271,10 +275,10 @@ extern "C" int moe_permute(const int32_t *ids, const void *x, int x_dtype, int64
   const int64_t row_bytes = d * 2;
   if (R <= kSmall) {
     if (row_bytes % 16 == 0)
-      permute_small_kernel<16><<<1, kSmall, 0, st>>>(ids, static_cast<const uint8_t *>(x), int(R), int(E), k, row_bytes,
+      launch_pdl(permute_small_kernel<16>, dim3(1), dim3(kSmall), 0, st, ids, static_cast<const uint8_t *>(x), int(R), int(E), k, row_bytes,
                                                      offsets, perm, inv_perm, static_cast<uint8_t *>(xp));
     else
-      permute_small_kernel<8><<<1, kSmall, 0, st>>>(ids, static_cast<const uint8_t *>(x), int(R), int(E), k, row_bytes,
+      launch_pdl(permute_small_kernel<8>, dim3(1), dim3(kSmall), 0, st, ids, static_cast<const uint8_t *>(x), int(R), int(E), k, row_bytes,
                                                     offsets, perm, inv_perm, static_cast<uint8_t *>(xp));
     return check_launch("permute_small");
   }
@@ -282,17 +286,17 @@ extern "C" int moe_permute(const int32_t *ids, const void *x, int x_dtype, int64
   int32_t *tile_counts = static_cast<int32_t *>(workspace);
   int32_t *tile_base = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) +
                                                    align256(size_t(ntiles) * size_t(E) * 4));
-  count_kernel<<<ntiles, kTile, 0, st>>>(ids, R, int(E), tile_counts);
+  launch_pdl(count_kernel, dim3(ntiles), dim3(kTile), 0, st, ids, R, int(E), tile_counts);
   const bool fused = int64_t(ntiles) * E <= kFusedScanMax;
-  if (!fused) scan_kernel<<<1, kMaxE, 0, st>>>(tile_counts, ntiles, int(E), tile_base, offsets);
+  if (!fused) launch_pdl(scan_kernel, dim3(1), dim3(kMaxE), 0, st, tile_counts, ntiles, int(E), tile_base, offsets);
   const int32_t *tb = fused ? nullptr : tile_base;
   const uint8_t *xb = static_cast<const uint8_t *>(x);
   uint8_t *xpb = static_cast<uint8_t *>(xp);
   if (row_bytes % 16 == 0)
-    scatter_kernel<16><<<ntiles * kSub, kTile, 0, st>>>(ids, tile_counts, tb, ntiles, xb, R, int(E), k, row_bytes,
+    launch_pdl(scatter_kernel<16>, dim3(ntiles * kSub), dim3(kTile), 0, st, ids, tile_counts, tb, ntiles, xb, R, int(E), k, row_bytes,
                                                         offsets, perm, inv_perm, xpb);
   else
-    scatter_kernel<8><<<ntiles * kSub, kTile, 0, st>>>(ids, tile_counts, tb, ntiles, xb, R, int(E), k, row_bytes,
+    launch_pdl(scatter_kernel<8>, dim3(ntiles * kSub), dim3(kTile), 0, st, ids, tile_counts, tb, ntiles, xb, R, int(E), k, row_bytes,
                                                        offsets, perm, inv_perm, xpb);
   return check_launch("permute");
 }

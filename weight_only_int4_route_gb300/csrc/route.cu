@@ -90,6 +90,7 @@ __global__ void __launch_bounds__(kThreads) route_f32_kernel(const T *__restrict
                                                               int T_, int d, int E, int k,
                                                               int renorm, int32_t *__restrict__ ids,
                                                               float *__restrict__ gates) {
+  pdl_enter();   // see launch_pdl
   __shared__ float xs[kTok][kKC];
   __shared__ float lg[kTok][kMaxE + 1];
   const int tid = threadIdx.x, warp = tid >> 5;
@@ -144,6 +145,7 @@ template <typename T, int kPEG>
 __global__ void __launch_bounds__(kThreads) route_partial_kernel(const T *__restrict__ x, const T *__restrict__ wr,
                                                                  int T_, int d, int E, int KS,
                                                                  float *__restrict__ part) {
+  pdl_enter();   // see launch_pdl
   __shared__ __align__(16) uint16_t xs[kPTok][kPKC + 8];
   __shared__ __align__(16) uint16_t ws[kPKC][kPEG + 8];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -259,6 +261,7 @@ __global__ void __launch_bounds__(kThreads) route_reduce_topk_kernel(const float
                                                                      int E, const float *__restrict__ bias, int k,
                                                                      int renorm, int32_t *__restrict__ ids,
                                                                      float *__restrict__ gates) {
+  pdl_enter();   // see launch_pdl
   __shared__ float lg[kThreads / 32][kMaxE];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int tok = blockIdx.x * (kThreads / 32) + warp;
@@ -288,6 +291,7 @@ __global__ void __launch_bounds__(kThreads * 2) route_reduce_small_kernel(const 
                                                                         int T_, int E, const float *__restrict__ bias,
                                                                         int k, int renorm, int32_t *__restrict__ ids,
                                                                         float *__restrict__ gates) {
+  pdl_enter();   // see launch_pdl
   constexpr int kW = kThreads * 2 / 32;
   __shared__ float red[kW][kMaxE];
   __shared__ float lg[kMaxE];
@@ -350,10 +354,10 @@ extern "C" int moe_route_topk(const void *x, int x_dtype, const void *w_router, 
   const unsigned grid = unsigned(cdiv(T, kTok));
   if (wr_dtype == MOE_F32) {
     if (x_dtype == MOE_F16)
-      route_f32_kernel<__half><<<grid, kThreads, 0, st>>>(static_cast<const __half *>(x),
+      launch_pdl(route_f32_kernel<__half>, dim3(grid), dim3(kThreads), 0, st, static_cast<const __half *>(x),
           static_cast<const float *>(w_router), bias, int(T), int(d), int(E), k, renormalize, ids, gate_w);
     else
-      route_f32_kernel<__nv_bfloat16><<<grid, kThreads, 0, st>>>(static_cast<const __nv_bfloat16 *>(x),
+      launch_pdl(route_f32_kernel<__nv_bfloat16>, dim3(grid), dim3(kThreads), 0, st, static_cast<const __nv_bfloat16 *>(x),
           static_cast<const float *>(w_router), bias, int(T), int(d), int(E), k, renormalize, ids, gate_w);
   } else {
     const size_t need = moe_route_topk_workspace_size(T, d, E);
@@ -367,19 +371,19 @@ extern "C" int moe_route_topk(const void *x, int x_dtype, const void *w_router, 
     const bool narrow = E <= 32;
     if (x_dtype == MOE_F16) {
       const __half *xh = static_cast<const __half *>(x), *wh = static_cast<const __half *>(w_router);
-      if (narrow) route_partial_kernel<__half, 32><<<pgrid, kThreads, 0, st>>>(xh, wh, int(T), int(d), int(E), KS, part);
-      else route_partial_kernel<__half, 64><<<pgrid, kThreads, 0, st>>>(xh, wh, int(T), int(d), int(E), KS, part);
+      if (narrow) launch_pdl(route_partial_kernel<__half, 32>, dim3(pgrid), dim3(kThreads), 0, st, xh, wh, int(T), int(d), int(E), KS, part);
+      else launch_pdl(route_partial_kernel<__half, 64>, dim3(pgrid), dim3(kThreads), 0, st, xh, wh, int(T), int(d), int(E), KS, part);
     } else {
       const __nv_bfloat16 *xb = static_cast<const __nv_bfloat16 *>(x), *wb = static_cast<const __nv_bfloat16 *>(w_router);
-      if (narrow) route_partial_kernel<__nv_bfloat16, 32><<<pgrid, kThreads, 0, st>>>(xb, wb, int(T), int(d), int(E), KS, part);
-      else route_partial_kernel<__nv_bfloat16, 64><<<pgrid, kThreads, 0, st>>>(xb, wb, int(T), int(d), int(E), KS, part);
+      if (narrow) launch_pdl(route_partial_kernel<__nv_bfloat16, 32>, dim3(pgrid), dim3(kThreads), 0, st, xb, wb, int(T), int(d), int(E), KS, part);
+      else launch_pdl(route_partial_kernel<__nv_bfloat16, 64>, dim3(pgrid), dim3(kThreads), 0, st, xb, wb, int(T), int(d), int(E), KS, part);
     }
     MOE_TRY(check_launch("route_partial"));
     if (S >= 8 && T <= int64_t(num_sms()) * 2)
-      route_reduce_small_kernel<<<unsigned(T), kThreads * 2, 0, st>>>(part, S, int(T), int(E), bias, k, renormalize,
+      launch_pdl(route_reduce_small_kernel, dim3(unsigned(T)), dim3(kThreads * 2), 0, st, part, S, int(T), int(E), bias, k, renormalize,
                                                                        ids, gate_w);
     else
-      route_reduce_topk_kernel<<<unsigned(cdiv(T, kThreads / 32)), kThreads, 0, st>>>(part, S, int(T), int(E), bias, k,
+      launch_pdl(route_reduce_topk_kernel, dim3(unsigned(cdiv(T, kThreads / 32))), dim3(kThreads), 0, st, part, S, int(T), int(E), bias, k,
                                                                                    renormalize, ids, gate_w);
   }
   return check_launch("route_topk");
