@@ -503,7 +503,9 @@ GemmPlan plan_gemv(int64_t R, int64_t E, int64_t K, int64_t N, int bits, int act
   pl.mt = bits != 16 ? 2 : 1;   // 16-bit weights: one m-tile keeps the ring small
   pl.ng = int(m16 / pl.mt);
   const int64_t nck = K / 128;
-  const double rc = std::ceil(active + 0.5 * double(R) / (8.0 * pl.nt));
+  // row chunks: one ragged tail per active expert on average, never more than the rows allow
+  const double rc = std::min(std::ceil(active + 0.5 * double(R) / (8.0 * pl.nt)),
+                             active - 1.0 + std::ceil(double(R) / (8.0 * pl.nt)));
   const int64_t warps = int64_t(num_sms()) * blocks_per_sm(false, bits, pl.nt, pl.mt, bits != 16) * kWarps;
   const double step_bytes = double(pl.mt) * 16 * 128 * bits / 8;   // weight bytes per warp per chunk
   const size_t kPartialCap = size_t(256) << 20;
