@@ -264,7 +264,13 @@ int moe_layer_routing_view(const moe_layer_desc *desc, int64_t T, void *workspac
                            moe_layer_routing *view);
 /* Number of kernels one moe_layer_forward(desc, T tokens) enqueues (0 if invalid or T == 0). */
 int moe_layer_launch_count(const moe_layer_desc *desc, int64_t T);
-/* x: (T, d) dtype; out: (T, d) dtype. */
+/* x: (T, d) dtype; out: (T, d) dtype.  With a shared expert (Fs > 0) the shared expert's kernels
+ * run on a second stream owned by the library (one per calling thread and device, created on
+ * first use), forked from `stream` before the router and joined back into `stream` before the
+ * combine: all work of the call is ordered after what was enqueued on `stream` before it, and
+ * everything enqueued on `stream` after it is ordered after all of it, as for a single-stream
+ * call; a capture of `stream` records both branches.  The kernels of the chain are launched with
+ * programmatic stream serialization (each waits for its predecessor before touching memory). */
 int moe_layer_forward(const moe_layer_desc *desc, const moe_layer_weights *w, const void *x,
                       int64_t T, void *out, void *workspace, size_t workspace_bytes,
                       moe_stream_t stream);

@@ -16,11 +16,13 @@
 // dequantized pairs and its B registers 8 bytes of the activation row.
 //
 // Work unit = (expert row chunk, channel group of MT m-tiles, K split).  Every warp walks its own
-// sequence of units with no block-level synchronization.  Each lane streams its own weight,
-// activation and scale bytes with cp.async into a private ring of kDepth chunk slots in shared
-// memory (no other lane reads them, so a wait_group is the only synchronization) and reads them
-// back right before the MMAs; the ring holds the bytes in flight without holding registers.  K
-// splits write fp32 partial sums that are summed later in split order.
+// sequence of units with no block-level synchronization.  The warp streams the unit's weight,
+// activation and scale bytes with cp.async into its own ring of kDepth chunk slots in shared
+// memory and reads them back right before the MMAs; the ring holds the bytes in flight without
+// holding registers.  Weight rows are copied warp-wide (consecutive lanes take consecutive
+// 16-byte pieces of a row, so every request fills whole sectors) and read by other lanes, so a
+// step waits for the lane's own copy group and then for the whole warp (__syncwarp).  K splits
+// write fp32 partial sums that are summed later in split order.
 #include <algorithm>
 #include <cmath>
 #include <mutex>
