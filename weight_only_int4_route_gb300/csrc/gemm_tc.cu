@@ -40,6 +40,7 @@
 #include <cuda.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "moe_internal.cuh"
 
@@ -688,15 +689,18 @@ int launch_typed(const GemmArgs &g, cudaStream_t st) {
   tp.act = g.act;
   tp.out_dtype = g.out_dtype;
   tp.swiglu = g.act == MOE_ACT_SWIGLU ? 1 : 0;
-  tp.ncb = tp.swiglu ? g.N / kBM : g.N / kBM;  // SwiGLU: 64 gate + 64 up channels per tile
+  tp.ncb = g.N / kBM;  // SwiGLU: 64 gate + 64 up channels per 128-channel block, the same count
   const size_t smem = smem_bytes(BITS);
-  static bool attr_set[2][3] = {{false, false, false}, {false, false, false}};
-  bool &done = attr_set[std::is_same<T, __half>::value ? 0 : 1][BITS == 4 ? 0 : (BITS == 8 ? 1 : 2)];
-  if (!done) {
+  // the shared-memory opt-in is a per-device attribute of the kernel: set once per device
+  static std::atomic<bool> attr_set[64];   // one per instance (template) and device
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return check_launch("gemm_tc: cudaGetDevice");
+  if (dev < 0 || dev >= 64) return set_error(MOE_ERR_UNSUPPORTED, "gemm_tc: device index %d >= 64", dev);
+  if (!attr_set[dev].load(std::memory_order_relaxed)) {
     if (cudaFuncSetAttribute(gemm_tc_kernel<T, BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
         cudaSuccess)
       return check_launch("gemm_tc attribute");
-    done = true;
+    attr_set[dev].store(true, std::memory_order_relaxed);
   }
   // tiles upper bound: (row tiles) x channel blocks
   const int64_t row_tiles = std::min<int64_t>(g.E, g.R) + cdiv(g.R, TB<BITS>::kBN);

@@ -457,15 +457,20 @@ Inst pick(bool bf, int bits, int nt, int mt, bool grouped) {
   return bf ? pick_t<__nv_bfloat16>(bits, nt, mt, grouped) : pick_t<__half>(bits, nt, mt, grouped);
 }
 
-// Resident blocks per SM of one instance (the dynamic shared memory opt-in is set on the way);
-// computed once per instance and device kind.
+// Resident blocks per SM of one instance (the dynamic shared memory opt-in, a per-device
+// attribute of the kernel, is set on the way); computed once per instance and device.
 int blocks_per_sm(bool bf, int bits, int nt, int mt, bool grouped) {
   static std::mutex mu;
-  static int cache[2][3][2][2][2] = {};
+  static int cache[64][2][3][2][2][2] = {};
   if (nt < 1 || nt > 2 || mt < 1 || mt > 2) return 1;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();   // the launch then reports the problem
+    return 1;
+  }
   const int bi = bits == 4 ? 0 : (bits == 8 ? 1 : 2);
   std::lock_guard<std::mutex> lock(mu);
-  int &c = cache[bf ? 1 : 0][bi][nt - 1][mt - 1][grouped ? 1 : 0];
+  int &c = cache[dev][bf ? 1 : 0][bi][nt - 1][mt - 1][grouped ? 1 : 0];
   if (c == 0) {
     const Inst in = pick(bf, bits, nt, mt, grouped);
     int nb = 0;
