@@ -9,8 +9,9 @@
 //   * A operand = dequantized weights, written by dequant warps straight into tensor memory
 //     (tcgen05.st), never through shared memory: shared-memory bandwidth is left to the
 //     activation operand.
-//   * B operand = up to 160 consecutive rows (128 for 16-bit weights) of the expert's segment of Xp, TMA-loaded with
-//     128-byte swizzle (K-major), so the MMA reads it through a shared-memory descriptor.
+//   * B operand = up to 160 consecutive rows (128 for 16-bit weights) of the expert's segment
+//     of Xp, TMA-loaded with 128-byte swizzle (K-major), so the MMA reads it through a
+//     shared-memory descriptor.
 //   * D = fp32 accumulator in tensor memory, double-buffered so the epilogue of one tile
 //     overlaps the mainloop of the next.
 //
@@ -36,7 +37,8 @@
 //
 // Every wait on an mbarrier is bounded (about two seconds); on expiry the CTA records an
 // error code in a device word, stops issuing work, drains its own asynchronous copies and
-// MMAs, frees its tensor memory and returns.
+// MMAs, frees its tensor memory and returns.  The kernel is launched with programmatic stream
+// serialization: its first act is to wait for the previous kernel in the stream (pdl_enter).
 #include <cuda.h>
 
 #include <algorithm>
