@@ -12,7 +12,7 @@ shares no code, table or constant with it.
             into the original BF16 tensor, bit for bit.
 
 BF16 layout (IEEE-754 binary32 truncated to its upper 16 bits): bit 15 sign, bits 14..7
-exponent (bias 127), bits 6..0 mantissa.  Readings of open points (also in the design doc):
+exponent (bias 127), bits 6..0 mantissa.  Readings of open points:
   * one exponent byte per element (the decompressed E-chunk is the plain byte array);
   * one SM byte per element: the sign in bit 7 and the 7 mantissa bits in bits 6..0 --
     8 bits per element is exactly byte-aligned, the plainest packing the page allows;

@@ -10,7 +10,7 @@ shares no code, table or constant with it.
              ELB(t)_cnt[j, e] = sum_i I[e in ELB_route[i, j]]; step (3): at a chunk boundary
              the planner snapshots the buffer and takes each layer's top-M experts.
 
-Readings of open points (also in the design doc):
+Readings of open points:
   * ELB_route[i, j] is the set of expert ids the draft routes to at step i in layer j (the
     k ids of that step's token); an expert counts once per step;
   * ids outside [0, E) are not counted;

@@ -17,7 +17,7 @@ itself: hand-computed Algorithm 1 tensors, exhaustive integer-to-float
 identities over every code, brute-force top-k, textbook stable sorting,
 closed forms of the activations and the E=1 dense-FFN reduction.
 
-Readings of open points (also listed in the design doc):
+Readings of open points:
   * Algorithm 1's W (E, M, N): M is the reduction (input) dim, N the output
     channel; per-channel scales are (E, 1, N).  Group-128 scales are
     (E, K/128, N) and scale rows g(m) = m // 128.  Scales carry the
