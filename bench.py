@@ -5,8 +5,9 @@ One step = one full pass of the layer (router + top-k, counting sort + permute, 
 fused dequant and activation, FC2, shared expert, un-permute/combine) over one batch of T
 synthetic tokens; for a stacked config (Phi-shaped, 32 layers) one step runs every layer.
 
-Default workload: the encoder-decoder MoE FFN (d=1024, ffn=4096, E=32, top-1, GELU,
-INT4 per-channel, fp16 activations) at T = 3840 tokens (40-token sentences x batch 96).
+Default workload: the largest single-GPU configuration, the Phi-3.5-MoE-shaped layer (d=4096,
+ffn=6400, E=16, top-2, SwiGLU, INT4 group-128, bf16 activations) at T = 8192 tokens, 32
+stacked layers with distinct weights run back to back on one stream per step.
 
 Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle instead, on a
 bounded token sample of the same workload.
@@ -35,6 +36,17 @@ METRIC = "MoE-layer tokens/s at 1 GB300; % of HBM (decode) / tensor (prefill) ro
 L2_BYTES = 129 * 1024 * 1024
 GRAPH_MAX_T = 32   # steps of at most this many tokens replay each layer's chain as a CUDA graph
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# A timed region at least this long runs under the sustained (power-capped) clocks; a shorter
+# one is compared with the burst tensor peak.
+SUSTAINED_REGION_S = 1.0
+
+
+def tensor_peak(peaks: dict, region_s: float, src: str):
+    """Dense 16-bit tensor peak that applies to a kernel timed inside a region of region_s seconds."""
+    if region_s >= SUSTAINED_REGION_S and "bf16_tflops_sustained" in peaks:
+        return peaks["bf16_tflops_sustained"], (f"{src} bf16 sustained (timed region {region_s:.2f} s >= "
+                                                f"{SUSTAINED_REGION_S:.0f} s)")
+    return peaks["bf16_tflops"], f"{src} bf16 burst (timed region {region_s:.2f} s < {SUSTAINED_REGION_S:.0f} s)"
 
 
 def parse():
@@ -43,7 +55,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="encdec_int4", choices=sorted(synth.CONFIGS))
+    ap.add_argument("--config", default="phi", choices=sorted(synth.CONFIGS))
     ap.add_argument("--T", type=int, default=0, help="tokens per step (default: the config's largest)")
     ap.add_argument("--layers", type=int, default=0, help="stacked layers per step (default: the config's)")
     ap.add_argument("--cpu-sample", type=int, default=256, help="tokens in the oracle's timed sample")
@@ -127,19 +139,22 @@ class ClockSampler:
         self.path = None
 
     def start(self):
+        self.error = None
         try:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
             self.f = open(self.path, "w")
+            self.ferr = tempfile.TemporaryFile(mode="w+")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
-                                          "--format=csv,noheader,nounits", "-lms", "50"],
-                                         stdout=self.f, stderr=subprocess.DEVNULL)
-        except Exception:
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=self.ferr)
+        except Exception as e:   # no nvidia-smi: the line says so instead of carrying clocks
             self.proc = None
+            self.error = f"nvidia-smi not started: {e}"
 
     def stop(self):
         if self.proc is None:
-            return None
+            return {"error": self.error} if self.error else None
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -153,8 +168,11 @@ class ClockSampler:
                 if len(parts) >= 9:
                     rows.append(parts)
         os.unlink(self.path)
+        self.ferr.seek(0)
+        err = self.ferr.read().strip()
+        self.ferr.close()
         if not rows:
-            return None
+            return {"error": "nvidia-smi gave no samples" + (f": {err[:200]}" if err else "")}
         sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
         mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
@@ -562,12 +580,14 @@ def main():
     dom_ms = st[dom]
     work = wm[dom]
     intensity = work["flops"] / work["bytes"]
-    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    # the stage times come from a run of args.steps profiled steps, as long as the timed region
+    tpeak, tpeak_src = tensor_peak(peaks, r["ms"] * args.steps * 1e-3, peak_src)
+    ridge = tpeak * 1e12 / (peaks["hbm_gbs"] * 1e9)
     if intensity >= ridge:
-        peak = peaks["bf16_tflops_sustained"] if "bf16_tflops_sustained" in peaks else peaks["bf16_tflops"]
+        peak = tpeak
         achieved = work["flops"] / (dom_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "peak_source": f"{peak_src} bf16 sustained (kernel timed inside back-to-back steps)"}
+                "peak_source": tpeak_src}
     else:
         peak = peaks["hbm_gbs"]
         achieved = work["bytes"] / (dom_ms * 1e-3) / 1e9
@@ -585,7 +605,7 @@ def main():
                                          if n_layers == 1 else f"{n_layers} distinct layers per step"),
                            active_experts=wm["active_experts"],
                            layer_roofline={"hbm_frac": lw["bytes"] / (layer_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                                           "tensor_frac": lw["flops"] / (layer_ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                                           "tensor_frac": lw["flops"] / (layer_ms * 1e-3) / 1e12 / tpeak,
                                            "bytes": lw["bytes"], "flops": lw["flops"]},
                            stage_ms=st, parallelism=f"replicas x{world} (token data parallel)"),
             "roofline": roof, "gpu_launches": r["launches"]}

@@ -324,14 +324,16 @@ def _check_layer(M, cfg, T, subset=None):
 
 
 @pytest.mark.parametrize("name,T", [("tiny", 16), ("tiny", 1), ("encdec_int8", 40), ("encdec_int4", 40),
-                                    ("encdec_int4", 77), ("encdec_int4", 1280), ("encdec_int8", 640),
-                                    ("qwen", 1), ("qwen", 8), ("qwen", 32), ("dsv2", 32), ("phi", 1), ("phi", 16)])
+                                    ("encdec_int4", 77), ("encdec_int8", 320), ("encdec_int4", 320),
+                                    ("encdec_int4", 1280), ("encdec_int8", 640),
+                                    ("qwen", 1), ("qwen", 8), ("qwen", 32), ("dsv2", 32), ("phi", 1), ("phi", 16),
+                                    ("phi", 32)])
 def test_layer_matches_oracle(M, name, T):
     _check_layer(M, synth.CONFIGS[name], T)
 
 
-@pytest.mark.parametrize("name,T", [("encdec_int4", 3840), ("encdec_int8", 1280), ("qwen", 4096),
-                                    ("dsv2", 512), ("phi", 8192)])
+@pytest.mark.parametrize("name,T", [("encdec_int4", 3840), ("encdec_int8", 3840), ("encdec_int8", 1280),
+                                    ("qwen", 4096), ("dsv2", 512), ("phi", 8192)])
 def test_layer_full_size_sampled(M, name, T):
     """Full workload size in the same launch configuration the benchmark times: routing
     compared in full, outputs on 256 seeded token samples (the layer is per-token
@@ -436,24 +438,86 @@ def PackedLayer_from(cfg, w):
 
 
 
-@pytest.mark.parametrize("name,T", [("qwen", 8), ("phi", 1), ("encdec_int4", 40)])
+@pytest.mark.parametrize("name,T", [("qwen", 8), ("phi", 1), ("encdec_int4", 40), ("dsv2", 32), ("qwen", 1)])
 def test_layer_graph_matches_forward(M, name, T):
     """The chain captured as one CUDA graph gives the eager forward's output bit for bit, also
-    after a new input is written into the graph's input buffer."""
+    after a new input is written into the graph's input buffer, and each replay matches the
+    float64 oracle (routing exactly, output within the layer tolerance)."""
     from weight_only_int4_route_gb300.moe import Layer, LayerGraph, PackedLayer
     cfg = synth.CONFIGS[name]
     w, x = layer_inputs(cfg, T)
     layer = Layer(PackedLayer.from_weights(cfg, w, DEV), T)
     g = LayerGraph(layer, T)
     for rep in range(2):
-        xi = x if rep == 0 else synth.normal(cfg, "x", (T, cfg.d), 1.0, cfg.torch_dtype, extra=99)
+        xi = x
+        if rep == 1:   # a second input, gap-filtered like the first
+            xi = O.gap_filtered(synth.normal(cfg, "x", (T, cfg.d), 1.0, cfg.torch_dtype, extra=99), w.wr, w.bias,
+                                cfg.k, lambda n, a: synth.redraw_rows(cfg, T + 99, n, a))
         g.x.copy_(xi.to(DEV))
         got = g.launch().clone()
+        torch.cuda.synchronize()
+        oracle = O.moe_layer(xi, w, cfg)
+        rt = layer.routing(T)
+        assert torch.equal(rt["ids"].cpu(), oracle["ids"]), rep
+        assert torch.equal(rt["perm"].cpu(), oracle["perm"]), rep
+        assert_close_layer(got.cpu(), oracle["out"], f"{name} T={T} graph replay {rep}")
         ref = layer.forward(xi.to(DEV))
         torch.cuda.synchronize()
         assert torch.equal(got, ref)
     assert M.device_error(DEV) == 0
     g.close()
+
+
+def _gap_filtered_all(cfg, x, weights, T):
+    """x with every token's top-(k+1) logits at least the test gap apart under each router."""
+    for _ in range(16):
+        before = x.clone()
+        for i, w in enumerate(weights):
+            x = O.gap_filtered(x, w.wr, w.bias, cfg.k, lambda n, a, i=i: synth.redraw_rows(cfg, T + 7 * i, n, a))
+        if torch.equal(before, x):
+            return x
+    raise RuntimeError("gap filter over several routers did not settle")
+
+
+@pytest.mark.slow
+def test_phi_stack_matches_oracle(M):
+    """The benchmark's step on the Phi-shaped stack: 32 layers with distinct weights, T = 8192,
+    one shared workspace, layers run back to back on one stream (each reads the same input and
+    writes its own output).  Layers 0 and 31 are drawn on the CPU so the oracle can recompute
+    them: routing compared in full, outputs on 256 seeded tokens each."""
+    from weight_only_int4_route_gb300.moe import Layer, PackedLayer
+    cfg = synth.CONFIGS["phi"]
+    T, L = 8192, cfg.layers
+    checked = {0: synth.layer_weights(cfg, 0), L - 1: synth.layer_weights(cfg, L - 1)}
+    x = _gap_filtered_all(cfg, synth.activations(cfg, T), list(checked.values()), T)
+    packed = []
+    for i in range(L):
+        wi = checked[i] if i in checked else synth.layer_weights(cfg, i, device=DEV)
+        packed.append(PackedLayer.from_weights(cfg, wi, DEV))
+        del wi
+    layers = [Layer(p, T) for p in packed[:1]]
+    ws = layers[0].ws
+    layers += [Layer(p, T, workspace=ws) for p in packed[1:]]
+    xd = x.to(DEV)
+    outs = [torch.empty((T, cfg.d), dtype=cfg.torch_dtype, device=DEV) for _ in range(L)]
+    for rep in range(2):   # a repeated step must give the same bits
+        for li, layer in enumerate(layers):
+            layer.forward(xd, outs[li])
+        torch.cuda.synchronize()
+        if rep == 0:
+            first = [outs[i].clone() for i in checked]
+    assert M.device_error(DEV) == 0
+    assert all(torch.equal(outs[i], f) for i, f in zip(checked, first))
+    subset = torch.randperm(T, generator=torch.Generator().manual_seed(31))[:256].sort().values
+    for i, w in checked.items():
+        ref = O.moe_layer(x, w, cfg, token_subset=subset)
+        # the shared workspace holds the routing of the last layer run
+        if i == L - 1:
+            rt = layers[i].routing(T)
+            assert torch.equal(rt["ids"].cpu(), ref["ids"])
+            assert torch.equal(rt["offsets"].cpu(), ref["offsets"])
+            assert torch.equal(rt["perm"].cpu(), ref["perm"])
+        assert_close_layer(outs[i].cpu()[subset], ref["out"], f"phi stack layer {i}")
 
 
 @pytest.mark.parametrize("name,T", [("qwen", 8), ("dsv2", 300)])

@@ -333,6 +333,34 @@ def test_gap_filter_removes_near_ties():
     assert bool(O.topk_gap_ok(O.router_logits(xf, w.wr, w.bias), cfg.k, 0.05).all())
 
 
+# ---------------------------------------------------------------- comparison metrics
+
+
+def test_rel_l2_hand_values():
+    """rel_l2(got, ref) = ||got - ref||_2 / ||ref||_2, by hand: got = (3, 4), ref = (0, 2) gives
+    ||(3, 2)|| / 2 = sqrt(13) / 2; got = ref gives 0; got = 0 gives 1; got = 2 ref gives 1."""
+    g, r = torch.tensor([3.0, 4.0]), torch.tensor([0.0, 2.0])
+    assert O.rel_l2(g, r) == pytest.approx(math.sqrt(13.0) / 2.0, rel=1e-15)
+    assert O.rel_l2(r, g) == pytest.approx(math.sqrt(13.0) / 5.0, rel=1e-15)   # not symmetric
+    x = torch.tensor([[1.5, -2.0], [0.25, 7.0]], dtype=torch.float64)
+    assert O.rel_l2(x, x) == 0.0
+    assert O.rel_l2(torch.zeros_like(x), x) == pytest.approx(1.0, rel=1e-15)
+    assert O.rel_l2(2 * x, x) == pytest.approx(1.0, rel=1e-15)
+    # a 2-D input is one vector: the Frobenius norm over every element
+    assert O.rel_l2(x + torch.tensor([[3.0, 0.0], [0.0, 4.0]]), x) == pytest.approx(
+        5.0 / math.sqrt(1.5 ** 2 + 2.0 ** 2 + 0.25 ** 2 + 7.0 ** 2), rel=1e-15)
+
+
+def test_max_abs_rel_hand_values():
+    """max_abs_rel(got, ref) = max|got - ref| / max|ref|, by hand: got = (3, 4), ref = (0, 2) gives
+    max(3, 2) / 2 = 1.5; a sign flip of the largest entry of ref = (1, -8) gives 16 / 8 = 2."""
+    g, r = torch.tensor([3.0, 4.0]), torch.tensor([0.0, 2.0])
+    assert O.max_abs_rel(g, r) == 1.5
+    assert O.max_abs_rel(r, g) == 0.75
+    assert O.max_abs_rel(torch.tensor([1.0, 8.0]), torch.tensor([1.0, -8.0])) == 2.0
+    assert O.max_abs_rel(r, r) == 0.0
+
+
 # ---------------------------------------------------------------- planted mistakes
 
 
@@ -378,3 +406,27 @@ def test_planted_missing_gate_is_caught(monkeypatch):
     monkeypatch.setattr(O, "gate_weights", lambda lg, ids, renormalize=False: torch.ones(ids.shape, dtype=torch.float64))
     with pytest.raises(AssertionError):
         test_gate_no_renorm_keeps_switch_prob_below_one()
+
+
+def test_planted_metric_denominator_swap_is_caught(monkeypatch):
+    """Dividing by the result under test instead of the reference would let a too-large output pass."""
+    monkeypatch.setattr(O, "rel_l2", lambda g, r: float(torch.linalg.vector_norm(g.double() - r.double())
+                                                       / torch.linalg.vector_norm(g.double())))
+    monkeypatch.setattr(O, "max_abs_rel", lambda g, r: float((g.double() - r.double()).abs().max()
+                                                            / g.double().abs().max()))
+    with pytest.raises(AssertionError):
+        test_rel_l2_hand_values()
+    with pytest.raises(AssertionError):
+        test_max_abs_rel_hand_values()
+
+
+def test_planted_vacuous_metric_is_caught(monkeypatch):
+    """A metric that compares the reference with itself (always 0) fails the hand values."""
+    monkeypatch.setattr(O, "rel_l2", lambda g, r: float(torch.linalg.vector_norm(r.double() - r.double())
+                                                       / torch.linalg.vector_norm(r.double())))
+    monkeypatch.setattr(O, "max_abs_rel", lambda g, r: float((r.double() - r.double()).abs().max()
+                                                            / r.double().abs().max()))
+    with pytest.raises(AssertionError):
+        test_rel_l2_hand_values()
+    with pytest.raises(AssertionError):
+        test_max_abs_rel_hand_values()
