@@ -49,7 +49,8 @@ typedef enum {
   MOE_ERR_INVALID_ARG = -1, /* null/misaligned pointer, bad size, bad enum */
   MOE_ERR_UNSUPPORTED = -2, /* valid but unsupported shape / dtype combination */
   MOE_ERR_WORKSPACE = -3,   /* workspace smaller than the matching *_workspace_size */
-  MOE_ERR_CUDA = -4         /* the CUDA runtime rejected a launch */
+  MOE_ERR_CUDA = -4,        /* the CUDA runtime rejected a launch */
+  MOE_ERR_DEVICE_CHECK = -5 /* checked build: a kernel found an out-of-range index (moe_check_status) */
 } moe_status;
 
 typedef enum { MOE_F16 = 0, MOE_BF16 = 1, MOE_F32 = 2 } moe_dtype;
@@ -68,6 +69,21 @@ int moe_version(void);
  * incomplete).  This call synchronizes `stream`, copies the code to *host_code (0 = no
  * error) and clears it. */
 int moe_device_error(moe_stream_t stream, int32_t *host_code);
+
+/* Bounds-checked build.  libmoe_checked.so is this library compiled with MOE_CHECKED=1: its
+ * kernels check every index they read from device memory before using it -- expert ids
+ * (moe_permute: in [0, E)), expert row offsets (grouped GEMMs: 0 <= offsets[e] <=
+ * offsets[e+1] <= R) and permutation entries (moe_unpermute_combine: inv_perm in [0, T*k)) --
+ * skip the access when one is out of range and record the kind of violation in a device
+ * check word; nothing faults and nothing traps.  A GEMM whose offsets fail the check computes
+ * nothing (its output is left as it was).  The plain build does none of these checks (see each
+ * call for what out-of-range input does there).
+ * moe_checked_build: 1 in the checked library, 0 in the plain one.
+ * moe_check_status: synchronizes `stream`, reads and clears the check word into *host_flags
+ * (bit 1: expert id, bit 2: offsets, bit 4: permutation entry; always 0 in the plain build)
+ * and returns MOE_ERR_DEVICE_CHECK if any bit is set, else MOE_OK. */
+int moe_checked_build(void);
+int moe_check_status(moe_stream_t stream, int32_t *host_flags);
 
 /* ------------------------------------------------------------------------------------
  * Weight packing.  [FT] Algorithm 1: W (E, M, N) integer codes, M = reduction dim,
@@ -138,7 +154,12 @@ int moe_route_topk(const void *x, int x_dtype, const void *w_router, int wr_dtyp
  *   xp[p, :] = x[perm[p] / k, :].
  * ids: int32 (T, k), every id in [0, E).  offsets: int32 (E+1).  perm, inv_perm: int32
  * (T*k).  xp: (T*k, d) x_dtype.  workspace: >= moe_permute_workspace_size(T, E, k) bytes
- * (may be NULL when that size is 0).  Out-of-range ids are undefined behaviour. */
+ * (may be NULL when that size is 0).
+ * Out-of-range ids (< 0 or >= E) are dropped: such a row gets no position, the offsets count
+ * only the rows with valid ids (offsets[E] is then below T*k), its inv_perm entry is -1 and
+ * perm entries from offsets[E] on are left unwritten; moe_unpermute_combine skips inv_perm
+ * entries outside [0, T*k), so a dropped row adds nothing to the output.  The checked build
+ * also sets bit 1 of the check word. */
 size_t moe_permute_workspace_size(int64_t T, int64_t E, int k);
 int moe_permute(const int32_t *ids, const void *x, int x_dtype, int64_t T, int64_t d, int64_t E,
                 int k, int32_t *offsets, int32_t *perm, int32_t *inv_perm, void *xp,
@@ -155,17 +176,21 @@ int moe_permute(const int32_t *ids, const void *x, int x_dtype, int64_t T, int64
  *                                     SWIGLU: silu(acc[:, :N/2]) * acc[:, N/2:] : (R, N/2)
  * a: (R, K) a_dtype (F16|BF16) row-major, R = total rows.  packed_w: from
  * moe_pack_weights with this (E, K, N, bits, group) and w_dtype == a_dtype.
- * offsets: int32 (E+1) device, non-decreasing, offsets[E] == R; NULL means one group
- * holding all R rows (then E must be 1).
+ * offsets: int32 (E+1) device, non-decreasing, offsets[E] <= R (output rows from offsets[E] on
+ * are left unspecified); NULL means one group holding all R rows (then E must be 1).  Offsets outside
+ * these rules are undefined behaviour in the plain build; the checked build computes nothing
+ * and sets bit 2 of the check word.
  * out_dtype: F16 | BF16 | F32.  With act NONE the output may be requested as fp32
  * split-K partials instead (see moe_grouped_gemm_partials).
  * workspace: >= moe_grouped_gemm_workspace_size(...) bytes.
  * Per-channel scales are applied to the fp32 accumulator (an exact reformulation of
  * Algorithm 1 up to rounding order); group-128 scales are applied in the mainloop as
  * RN(q * s) in the operand dtype, as Algorithm 1 states. */
-/* Which kernel a grouped GEMM with these arguments (offsets given) runs: 1 = the tcgen05
- * tensor-memory kernel (>= 64 rows per active expert), 2 = the decode weight-stream kernel
- * (<= 32 rows per active expert), 0 = the warp-MMA tile kernel (in between). */
+/* Which kernel a grouped GEMM with these arguments (offsets given) runs, judged from the
+ * average rows per active expert a = ceil(R / min(E, R)): 2 = the decode weight-stream kernel
+ * (a <= 16); 1 = the tcgen05 tensor-memory kernel (a >= 17 for 4- and 8-bit weights, a >= 64
+ * for 16-bit weights, when the shape suits it: K % 128 == 0, N % 128 == 0, or for SWIGLU
+ * (N/2) % 64 == 0); 0 = the warp-MMA tile kernel (the rest). */
 int moe_gemm_path(int64_t R, int64_t E, int64_t K, int64_t N, int bits, int group, int act);
 size_t moe_grouped_gemm_workspace_size(int64_t R, int64_t E, int64_t K, int64_t N, int bits,
                                        int act);
@@ -187,7 +212,10 @@ int moe_grouped_gemm_w8a16(const void *a, int a_dtype, const void *packed_w, int
  * (moe_grouped_gemm_workspace_size > 2 MiB) return MOE_ERR_UNSUPPORTED without launching.
  * Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.  The first call on
  * a device looks up the array's device address (cudaGetSymbolAddress) with that device
- * current; make that first call before any stream capture.  Every call on a device shares the
+ * current; make that first call before any stream capture.  The address is kept per device
+ * index and belongs to the device's primary context (the one the CUDA runtime uses): a caller
+ * that runs this call under a context of its own, or after resetting the device
+ * (cudaDeviceReset), must not use it.  Every call on a device shares the
  * one array and leaves its last contents there (each call overwrites every partial it reads,
  * so nothing needs clearing); calls that overlap on the GPU (different streams, or several
  * host threads) race on it and must be serialized by the caller. */
@@ -204,7 +232,9 @@ int moe_grouped_gemm_w16a16(const void *a, int a_dtype, const void *packed_w, in
  * Un-permute and combine.  [FT] workflow: restore the row order and apply expert_scale;
  * [Specter] step 5: scatter back to the original positions.
  *   out[t, c] = sum_{j<k} gate_w[t, j] * yp[inv_perm[t*k + j], c]  (+ shared[t, c])
- * summed in fp32 in j order, rounded once to out_dtype.
+ * summed in fp32 in j order, rounded once to out_dtype.  An inv_perm entry outside
+ * [0, T*k) (a row moe_permute dropped) contributes nothing; the checked build also sets bit 4
+ * of the check word.
  * yp: (T*k, d) yp_dtype (F32|F16|BF16).  shared: (T, d) shared_dtype or NULL.
  * out: (T, d) out_dtype (F16|BF16|F32). */
 int moe_unpermute_combine(const void *yp, int yp_dtype, const int32_t *inv_perm,

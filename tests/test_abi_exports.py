@@ -23,6 +23,17 @@ def test_every_header_symbol_is_exported(L):
     assert set(names) == set(M._SIGS), "binding and header disagree"
 
 
+def test_checked_library_exports_the_same_symbols():
+    """The bounds-checked build (MOE_CHECKED=1) is the same ABI: every header symbol, and it
+    says that it is the checked build (the plain one says it is not)."""
+    B.build(checked=True)
+    C = M.lib_checked()
+    assert [n for n in M.header_symbols() if not hasattr(C, n)] == []
+    assert C.moe_checked_build() == 1
+    assert M.lib().moe_checked_build() == 0
+    assert C.moe_check_status(None, None) == -1   # host_flags NULL: refused on the host
+
+
 def test_version_and_error_string(L):
     assert L.moe_version() == 1
     assert isinstance(L.moe_last_error_string(), bytes)

@@ -237,6 +237,27 @@ extern "C" int moe_device_error(moe_stream_t stream, int32_t *host_code) {
 }
 extern "C" int moe_version(void) { return 1; }
 
+extern "C" int moe_checked_build(void) { return MOE_CHECKED; }
+
+extern "C" int moe_check_status(moe_stream_t stream, int32_t *host_flags) {
+  MOE_REQUIRE(host_flags != nullptr, "host_flags is NULL");
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return check_launch("check status: stream synchronize");
+  int v = 0;
+  MOE_TRY(check_word_take_permute(&v));
+  MOE_TRY(check_word_take_combine(&v));
+  MOE_TRY(check_word_take_gemm_tc(&v));
+  MOE_TRY(check_word_take_gemv(&v));
+  MOE_TRY(check_word_take_gemm_mma(&v));
+  *host_flags = v;
+  if (v != 0)
+    return set_error(MOE_ERR_DEVICE_CHECK, "device bounds check failed (flags 0x%x:%s%s%s)", v,
+                     (v & kCheckExpertId) ? " expert id out of range" : "",
+                     (v & kCheckOffsets) ? " expert offsets unusable" : "",
+                     (v & kCheckPerm) ? " permutation entry out of range" : "");
+  return MOE_OK;
+}
+
 extern "C" int moe_gemm_path(int64_t R, int64_t E, int64_t K, int64_t N, int bits, int group, int act) {
   if (R <= 0 || E < 1 || K < 128 || N < 64) return 0;
   const GemmPlan pl = plan_gemm(R, E, K, N, bits, act, false);

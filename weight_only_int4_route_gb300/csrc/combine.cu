@@ -7,6 +7,9 @@
 #include "moe_internal.cuh"
 
 namespace moe {
+
+MOE_DEFINE_CHECK_WORD(combine)
+
 namespace {
 
 __device__ __forceinline__ void st_any(void *p, int dt, int64_t i, float v) {
@@ -118,7 +121,10 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(
         if (l < nent && tok < T) {
           pl = inv_perm[tok * k + l % k];
           gl = gate[tok * k + l % k];
-          if (pl < 0 || pl >= R) pl = -1;   // malformed permutation: contributes nothing
+          if (pl < 0 || pl >= R) {   // dropped row (or a malformed permutation): contributes nothing
+            if (MOE_CHECKED) check_fail(kCheckPerm);
+            pl = -1;
+          }
         }
       }
       const int nj = nent - jb < 32 ? nent - jb : 32;
@@ -269,7 +275,10 @@ __global__ void __launch_bounds__(kSmallWarps * 32) combine_small_kernel(
   if (lane < k) {
     pl = inv_perm[tok * k + lane];
     gl = gate[tok * k + lane];
-    if (pl < 0 || pl >= R) pl = -1;   // malformed permutation: contributes nothing
+    if (pl < 0 || pl >= R) {   // dropped row (or a malformed permutation): contributes nothing
+      if (MOE_CHECKED) check_fail(kCheckPerm);
+      pl = -1;
+    }
   }
   const int ny = k * ysplits;
   const int nterms = ny + (sh ? shsplits : 0);

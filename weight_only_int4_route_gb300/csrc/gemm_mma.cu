@@ -29,6 +29,9 @@
 #include "moe_internal.cuh"
 
 namespace moe {
+
+MOE_DEFINE_CHECK_WORD(gemm_mma)
+
 namespace {
 
 constexpr int kWarps = 8;
@@ -136,7 +139,9 @@ __global__ void __launch_bounds__(kThreads) gemm_mma_kernel(const KParams p) {
 
   // ---- per-expert row-tile table (prefix over experts of ceil(rows / MT)) ----
   int cnt = 0;
-  if (tid < E) {
+  // checked build: unusable offsets leave the kernel without tiles (nothing is read or written)
+  const bool off_ok = p.offsets == nullptr || offsets_usable(p.offsets, E, p.R, [] { check_fail(kCheckOffsets); });
+  if (tid < E && off_ok) {
     const int o0 = p.offsets ? p.offsets[tid] : 0;
     const int o1 = p.offsets ? p.offsets[tid + 1] : p.R;
     cnt = (o1 - o0 + MT - 1) / MT;

@@ -50,6 +50,8 @@ namespace moe {
 
 __device__ int g_moe_device_error = 0;
 
+MOE_DEFINE_CHECK_WORD(gemm_tc)
+
 namespace {
 
 constexpr int kEpiWarps = 8;        // epilogue warps (two per TMEM lane quarter)
@@ -376,7 +378,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::);
   }
   int cnt = 0;
-  if (tid < E) {   // no offsets array: one expert owning all R rows
+  // checked build: unusable offsets leave the kernel without tiles (nothing is read or written)
+  const bool off_ok = p.offsets == nullptr || offsets_usable(p.offsets, E, p.R, [] { check_fail(kCheckOffsets); });
+  if (tid < E && off_ok) {   // no offsets array: one expert owning all R rows
     const int o0 = p.offsets ? p.offsets[tid] : 0, o1 = p.offsets ? p.offsets[tid + 1] : p.R;
     cnt = ((o1 - o0 + kBN - 1) / kBN) * p.ncb;
     s_off[tid] = o0;

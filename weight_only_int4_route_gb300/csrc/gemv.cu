@@ -30,6 +30,9 @@
 #include "moe_internal.cuh"
 
 namespace moe {
+
+MOE_DEFINE_CHECK_WORD(gemv)
+
 namespace {
 
 constexpr int kWarps = 4;
@@ -177,10 +180,12 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const GvParams p) {
 
   // row chunks per expert and their exclusive prefix (each thread takes two consecutive experts)
   int cnt[2] = {0, 0};
+  // checked build: unusable offsets leave the kernel without units (nothing is read or written)
+  const bool off_ok = p.offsets == nullptr || offsets_usable(p.offsets, E, p.R, [] { check_fail(kCheckOffsets); });
 #pragma unroll
   for (int q = 0; q < 2; ++q) {
     const int e = 2 * tid + q;
-    if (e < E) {
+    if (e < E && off_ok) {
       const int o0 = p.offsets ? p.offsets[e] : 0;
       const int o1 = p.offsets ? p.offsets[e + 1] : p.R;
       cnt[q] = (o1 - o0 + 8 * NT - 1) / (8 * NT);

@@ -8,7 +8,44 @@
 
 #include "moe.h"
 
+// Checked build (compiled with -DMOE_CHECKED=1 into a separate library): kernels bounds-check
+// the indices they read from device memory -- expert ids, expert row offsets, permutation
+// entries -- skip the access when one is out of range and record the kind of violation in a
+// device check word (moe_check_status reads it).  The plain build checks nothing beyond what
+// its documented behaviour needs.
+#ifndef MOE_CHECKED
+#define MOE_CHECKED 0
+#endif
+
 namespace moe {
+
+// Bits of the device check word.
+enum : int { kCheckExpertId = 1, kCheckOffsets = 2, kCheckPerm = 4 };
+
+// One check word per translation unit (device variables are not shared across separately
+// compiled files); check_word_take_<tu> ORs the word into *out and clears it.
+#define MOE_DEFINE_CHECK_WORD(tu)                                                               \
+  namespace {                                                                                   \
+  __device__ int g_check_word = 0;                                                              \
+  __device__ __forceinline__ void check_fail(int bit) { atomicOr(&g_check_word, bit); }         \
+  }                                                                                             \
+  int check_word_take_##tu(int *out) {                                                          \
+    int v = 0;                                                                                  \
+    if (cudaMemcpyFromSymbol(&v, g_check_word, sizeof(int)) != cudaSuccess)                     \
+      return check_launch("check word read");                                                   \
+    if (v != 0) {                                                                               \
+      const int zero = 0;                                                                       \
+      if (cudaMemcpyToSymbol(g_check_word, &zero, sizeof(int)) != cudaSuccess)                  \
+        return check_launch("check word reset");                                                \
+    }                                                                                           \
+    *out |= v;                                                                                  \
+    return MOE_OK;                                                                              \
+  }
+int check_word_take_permute(int *out);
+int check_word_take_combine(int *out);
+int check_word_take_gemm_tc(int *out);
+int check_word_take_gemv(int *out);
+int check_word_take_gemm_mma(int *out);
 
 // ---------------------------------------------------------------- host side
 
@@ -335,6 +372,25 @@ __device__ __forceinline__ void act_silu2(float &x0, float &x1) {
 }
 __device__ __forceinline__ float act_apply(float x, int act) {
   return act == MOE_ACT_RELU ? act_relu(x) : (act == MOE_ACT_GELU ? act_gelu(x) : x);
+}
+
+// Checked build: whether the expert row offsets are usable (0 <= off[e] <= off[e+1] <= R for
+// every e < E).  Every thread of the block must call it (it contains a barrier); a thread
+// whose expert entry is bad calls fail().  In the plain build it is true without a look.
+template <typename Fail>
+__device__ __forceinline__ bool offsets_usable(const int32_t *off, int E, int64_t R, Fail fail) {
+#if MOE_CHECKED
+  int bad = 0;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int o0 = off[e], o1 = off[e + 1];
+    bad |= (o0 < 0 || o1 < o0 || int64_t(o1) > R) ? 1 : 0;
+  }
+  if (bad) fail();
+  return __syncthreads_or(bad) == 0;
+#else
+  (void)off; (void)E; (void)R; (void)fail;
+  return true;
+#endif
 }
 
 __device__ __forceinline__ void pdl_enter() {

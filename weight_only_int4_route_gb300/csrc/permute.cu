@@ -18,6 +18,9 @@
 #include "moe_internal.cuh"
 
 namespace moe {
+
+MOE_DEFINE_CHECK_WORD(permute)
+
 namespace {
 
 constexpr int kTile = 256;
@@ -35,6 +38,7 @@ __global__ void __launch_bounds__(kTile) count_kernel(const int32_t *__restrict_
   if (f < R) {
     const int e = ids[f];
     if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);  // out-of-range ids are dropped
+    else if (MOE_CHECKED) check_fail(kCheckExpertId);
   }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += kTile) tile_counts[int64_t(blockIdx.x) * E + e] = cnt[e];
@@ -151,7 +155,7 @@ __global__ void __launch_bounds__(kTile) scatter_kernel(const int32_t *__restric
   }
   const int64_t f = int64_t(tile) * kTile + threadIdx.x;
   int e = f < R ? ids[f] : -1;
-  if (e >= E) e = -1;
+  if (e < 0 || e >= E) e = -1;
   const unsigned same = __match_any_sync(0xffffffffu, e);
   const int rank_in_warp = __popc(same & ((1u << lane) - 1u));
   if (e >= 0 && rank_in_warp == 0) wcount[warp][e] = __popc(same);
@@ -165,6 +169,8 @@ __global__ void __launch_bounds__(kTile) scatter_kernel(const int32_t *__restric
       inv_perm[f] = p;
     }
     dest[threadIdx.x] = p;
+  } else if (sub == 0 && f < R) {
+    inv_perm[f] = -1;   // dropped row: no position
   }
   __syncthreads();
   // gather this CTA's slice of the tile's rows: one warp per row
@@ -198,7 +204,11 @@ __global__ void __launch_bounds__(kSmall) permute_small_kernel(const int32_t *__
   for (int i = tid; i < (kSmall / 32) * E; i += kSmall) wcount[i / E][i % E] = 0;
   __syncthreads();
   int e = tid < R ? ids[tid] : -1;
-  if (e >= E) e = -1;
+  if (tid < R && (e < 0 || e >= E)) {
+    e = -1;
+    inv_perm[tid] = -1;   // dropped row: no position
+    if (MOE_CHECKED) check_fail(kCheckExpertId);
+  }
   const unsigned same = __match_any_sync(0xffffffffu, e);
   const int rank_in_warp = __popc(same & ((1u << lane) - 1u));
   if (e >= 0 && rank_in_warp == 0) wcount[warp][e] = __popc(same);

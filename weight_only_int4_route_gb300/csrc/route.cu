@@ -82,7 +82,12 @@ __device__ void topk_softmax_warp(const float *logits, int E, int k, int renorm,
   }
 }
 
-// fp32 router weights: fp32 FMA logits (small routers).
+// fp32 router weights: fp32 FMA logits (small routers).  CTA = kTok tokens; the (token,
+// expert) pairs are spread over the threads (expert fastest, so a warp reads consecutive
+// weights), and each reduction chunk of x and of the router weights is staged in shared memory
+// with coalesced loads; a chunk holds at most kWChunk weights, so few experts give long chunks.
+constexpr int kWChunk = 2048;
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads) route_f32_kernel(const T *__restrict__ x,
                                                               const float *__restrict__ wr,
@@ -91,28 +96,33 @@ __global__ void __launch_bounds__(kThreads) route_f32_kernel(const T *__restrict
                                                               int renorm, int32_t *__restrict__ ids,
                                                               float *__restrict__ gates) {
   pdl_enter();   // see launch_pdl
-  __shared__ float xs[kTok][kKC];
+  __shared__ float ws[kWChunk];
+  __shared__ float xs[kTok][kWChunk / 16];
   __shared__ float lg[kTok][kMaxE + 1];
   const int tid = threadIdx.x, warp = tid >> 5;
   const int tok0 = blockIdx.x * kTok;
+  // rows of Wr per chunk: as many as fit kWChunk weights, at most the xs width
+  const int rows = min(kWChunk / 16, kWChunk / E);
   constexpr int kPairs = kTok * kMaxE / kThreads;
+  const int npairs = kTok * E;
   float acc[kPairs];
 #pragma unroll
   for (int i = 0; i < kPairs; ++i) acc[i] = 0.f;
-  for (int k0 = 0; k0 < d; k0 += kKC) {
-    const int kc = min(kKC, d - k0);
-    for (int i = tid; i < kTok * kKC; i += kThreads) {
-      const int r = i / kKC, c = i % kKC;
-      xs[r][c] = (tok0 + r < T_ && c < kc) ? to_f32(x[int64_t(tok0 + r) * d + k0 + c]) : 0.f;
+  for (int k0 = 0; k0 < d; k0 += rows) {
+    const int kc = min(rows, d - k0);
+    for (int i = tid; i < kc * E; i += kThreads) ws[i] = wr[int64_t(k0) * E + i];
+    for (int i = tid; i < kTok * kc; i += kThreads) {
+      const int r = i / kc, c = i % kc;
+      xs[r][c] = tok0 + r < T_ ? to_f32(x[int64_t(tok0 + r) * d + k0 + c]) : 0.f;
     }
     __syncthreads();
 #pragma unroll
     for (int i = 0; i < kPairs; ++i) {
       const int pidx = tid + i * kThreads;
-      const int r = pidx / kMaxE, e = pidx % kMaxE;
-      if (e < E) {
+      if (pidx < npairs) {
+        const int r = pidx / E, e = pidx - r * E;
         float s = acc[i];
-        for (int c = 0; c < kc; ++c) s = fmaf(xs[r][c], wr[int64_t(k0 + c) * E + e], s);
+        for (int c = 0; c < kc; ++c) s = fmaf(xs[r][c], ws[c * E + e], s);
         acc[i] = s;
       }
     }
@@ -121,8 +131,10 @@ __global__ void __launch_bounds__(kThreads) route_f32_kernel(const T *__restrict
 #pragma unroll
   for (int i = 0; i < kPairs; ++i) {
     const int pidx = tid + i * kThreads;
-    const int r = pidx / kMaxE, e = pidx % kMaxE;
-    if (e < E) lg[r][e] = acc[i] + (bias ? bias[e] : 0.f);
+    if (pidx < npairs) {
+      const int r = pidx / E, e = pidx - r * E;
+      lg[r][e] = acc[i] + (bias ? bias[e] : 0.f);
+    }
   }
   __syncthreads();
   for (int r = warp; r < kTok; r += kThreads / 32) {

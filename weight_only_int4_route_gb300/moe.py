@@ -17,6 +17,7 @@ import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmoe.so")
+LIB_CHECKED_PATH = os.path.join(_PKG, "libmoe_checked.so")
 HEADER = os.path.join(os.path.dirname(_PKG), "include", "moe.h")
 
 F16, BF16, F32 = 0, 1, 2
@@ -52,6 +53,8 @@ _SIGS = {
     "moe_last_error_string": (ctypes.c_char_p, []),
     "moe_version": (_c_int, []),
     "moe_device_error": (_c_int, [_vp, ctypes.POINTER(ctypes.c_int32)]),
+    "moe_checked_build": (_c_int, []),
+    "moe_check_status": (_c_int, [_vp, ctypes.POINTER(ctypes.c_int32)]),
     "moe_packed_size": (_c_size, [_c_i64, _c_i64, _c_i64, _c_int, _c_int]),
     "moe_packed_scale_offset": (_c_size, [_c_i64, _c_i64, _c_i64, _c_int]),
     "moe_pack_weights": (_c_int, [_vp, _vp, _c_int, _c_i64, _c_i64, _c_i64, _c_int, _c_int, _vp, _c_size, _vp]),
@@ -90,6 +93,7 @@ _SIGS = {
 STAGES = ("start", "routed", "permuted", "fc1", "fc2", "shared", "done")
 
 _lib: Optional[ctypes.CDLL] = None
+_lib_checked: Optional[ctypes.CDLL] = None
 
 
 def header_symbols() -> list[str]:
@@ -98,19 +102,40 @@ def header_symbols() -> list[str]:
     return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", text)))
 
 
+def _load(path: str) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise RuntimeError(f"{os.path.basename(path)} is not built ({path}); run weight_only_int4_route_gb300/build.py "
+                           "or __graft_entry__.build() -- there is no fallback path")
+    L = ctypes.CDLL(path)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    return L
+
+
 def lib() -> ctypes.CDLL:
+    """The library (libmoe.so)."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError(f"libmoe.so is not built ({LIB_PATH}); run weight_only_int4_route_gb300/build.py "
-                               "or __graft_entry__.build() -- there is no fallback path")
-        L = ctypes.CDLL(LIB_PATH)
-        for name, (res, args) in _SIGS.items():
-            fn = getattr(L, name)
-            fn.restype = res
-            fn.argtypes = args
-        _lib = L
+        _lib = _load(LIB_PATH)
     return _lib
+
+
+def lib_checked() -> ctypes.CDLL:
+    """The bounds-checked build of the same library (libmoe_checked.so), for tests and debugging."""
+    global _lib_checked
+    if _lib_checked is None:
+        _lib_checked = _load(LIB_CHECKED_PATH)
+    return _lib_checked
+
+
+def check_status(device="cuda:0", L: Optional[ctypes.CDLL] = None) -> tuple[int, int]:
+    """(status, flags) of moe_check_status on the current stream: synchronizes, reads and clears
+    the library's device check word (always 0 in the plain build)."""
+    v = ctypes.c_int32(0)
+    st = (L or lib()).moe_check_status(_stream(torch.device(device)), ctypes.byref(v))
+    return int(st), int(v.value)
 
 
 def _check(st: int, what: str):
