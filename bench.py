@@ -62,6 +62,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="decode-sized steps: launch kernels one by one")
+    ap.add_argument("--decode-chain", action="store_true",
+                    help="decode-sized steps: the chain of kernels instead of the one-launch layer")
     ap.add_argument("--elb", action="store_true",
                     help="time ELB counting + top-M for one chunk boundary instead of the layer (separate metric)")
     ap.add_argument("--codec", action="store_true",
@@ -191,6 +193,8 @@ def run_ours(args, cfg, T, n_layers, world, rank, local):
     B.build()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    if args.decode_chain:
+        M.set_decode_mode("chain")
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -371,6 +375,7 @@ def run_ours(args, cfg, T, n_layers, world, rank, local):
     offs = layers[0].routing(T)["offsets"].cpu().tolist()
     counts = [offs[i + 1] - offs[i] for i in range(cfg.E)]
     launches_per_layer = layers[0].launch_count(T)
+    one_launch = launches_per_layer == 1
     # a kernel that gave up on a bounded wait leaves a code in the device error word: the run's
     # outputs and times are then not valid, so no number is reported
     derr = M.device_error(dev)
@@ -389,7 +394,10 @@ def run_ours(args, cfg, T, n_layers, world, rank, local):
     for g in graphs:
         g.close()
     return dict(ms=ms, stage_ms=stage_ms, counts=counts, clocks=clk, e2e=e2e, copies=copies,
-                launch="one CUDA graph per layer chain" if use_graph else "kernels launched one by one",
+                launch=("one kernel launch per layer" + (" (replayed from a CUDA graph)" if use_graph else "")
+                        if one_launch else
+                        "one CUDA graph per layer chain" if use_graph else "kernels launched one by one"),
+                one_launch=one_launch,
                 launches=launches_per_layer * n_layers * args.steps, per_layer_bytes=per_layer, kernels=kernels,
                 est_touch=est_touch, dist=dist)
 
@@ -574,11 +582,14 @@ def main():
     peaks, peak_src = load_peaks()
     wm = work_model(cfg, T, r["counts"])
     value = job_tokens_per_s(world, T, r["ms"])
-    # dominant kernel: the longer of the two grouped GEMM stages
+    # dominant kernel: the longer of the two grouped GEMM stages; a decode step that runs as one
+    # launch is its own dominant kernel (the whole layer's bytes over the layer's time)
     st = r["stage_ms"]
     dom = "fc1" if st["fc1"] >= st["fc2"] else "fc2"
     dom_ms = st[dom]
     work = wm[dom]
+    if r["one_launch"]:
+        dom, dom_ms, work = "layer", r["ms"] / n_layers, wm["layer"]
     intensity = work["flops"] / work["bytes"]
     # the stage times come from a run of args.steps profiled steps, as long as the timed region
     tpeak, tpeak_src = tensor_peak(peaks, r["ms"] * args.steps * 1e-3, peak_src)
@@ -593,8 +604,9 @@ def main():
         achieved = work["bytes"] / (dom_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "peak_source": f"{peak_src} HBM copy bandwidth"}
-    roof.update({"traffic": MEASURED_TRAFFIC.get((cfg.name, T, dom)) if n_layers == 1 else None,
-                 "kernel": f"grouped GEMM {dom.upper()} ({r['kernels'][dom]})",
+    roof.update({"traffic": MEASURED_TRAFFIC.get((cfg.name, T, dom)),
+                 "kernel": ("decode_layer_kernel (the whole layer in one launch)" if dom == "layer" else
+                            f"grouped GEMM {dom.upper()} ({r['kernels'][dom]})"),
                  "algorithmic_bytes": work["bytes"], "algorithmic_flops": work["flops"], "ms_per_launch": dom_ms})
     layer_ms = r["ms"] / n_layers
     lw = wm["layer"]
@@ -607,7 +619,8 @@ def main():
                            layer_roofline={"hbm_frac": lw["bytes"] / (layer_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
                                            "tensor_frac": lw["flops"] / (layer_ms * 1e-3) / 1e12 / tpeak,
                                            "bytes": lw["bytes"], "flops": lw["flops"]},
-                           stage_ms=st, parallelism=f"replicas x{world} (token data parallel)"),
+                           **({"stage_ms_kernel_chain": st} if r["one_launch"] else {"stage_ms": st}),
+                           parallelism=f"replicas x{world} (token data parallel)"),
             "roofline": roof, "gpu_launches": r["launches"]}
     if r["clocks"]:
         line["clocks"] = r["clocks"]

@@ -534,11 +534,15 @@ def test_forked_shared_expert_matches_serial(M, name, T):
     events = [torch.cuda.Event(enable_timing=True) for _ in STAGES]
     for e in events:   # torch creates the CUDA event on its first record
         e.record()
-    serial = layer.forward_profiled(xd, torch.empty((T, cfg.d), dtype=x.dtype, device=DEV), events).clone()
-    for _ in range(3):
-        forked = layer.forward(xd)
-        torch.cuda.synchronize()
-        assert torch.equal(forked, serial)
+    prev = M.set_decode_mode("chain")   # the kernel chain, also for a decode-sized T
+    try:
+        serial = layer.forward_profiled(xd, torch.empty((T, cfg.d), dtype=x.dtype, device=DEV), events).clone()
+        for _ in range(3):
+            forked = layer.forward(xd)
+            torch.cuda.synchronize()
+            assert torch.equal(forked, serial)
+    finally:
+        M.set_decode_mode(prev)
     assert M.device_error(DEV) == 0
 
 

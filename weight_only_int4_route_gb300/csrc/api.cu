@@ -4,6 +4,7 @@
 #include <stdio.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "moe_internal.cuh"
 
@@ -108,8 +109,13 @@ struct LayerPlan {
   int64_t T, R;
   GemmPlan fc1, fc2, sh1, sh2;
   bool fused_combine;   // top-1, no shared expert, FC2 on tcgen05: FC2 writes the layer output
-  size_t o_ids, o_gate, o_off, o_perm, o_inv, o_rws, o_pws, o_xp, o_p1, o_h, o_y, o_hs, o_ps1, o_ys, total;
+  DecodePlan dec;       // the one-launch decode layer (dec.ok: it takes this T)
+  size_t o_ids, o_gate, o_off, o_perm, o_inv, o_rws, o_pws, o_xp, o_p1, o_h, o_y, o_hs, o_ps1, o_ys, o_dec, total;
 };
+
+// 0: a decode step (T <= 32 on a supported layer) runs as one launch; 1: always the chain of
+// kernels (moe_set_decode_mode).
+std::atomic<int> g_decode_mode{0};
 
 int check_desc(const moe_layer_desc *d) {
   MOE_REQUIRE(d != nullptr, "desc is NULL");
@@ -125,7 +131,7 @@ int check_desc(const moe_layer_desc *d) {
   return MOE_OK;
 }
 
-LayerPlan plan_layer(const moe_layer_desc *d, int64_t T) {
+LayerPlan plan_layer(const moe_layer_desc *d, int64_t T, bool for_size = false) {
   LayerPlan p{};
   p.T = T;
   p.R = T * d->k;
@@ -160,9 +166,22 @@ LayerPlan plan_layer(const moe_layer_desc *d, int64_t T) {
     p.o_ps1 = take(p.sh1.partial ? size_t(p.sh1.splits) * T * 2 * d->Fs * 4 : 0);
     p.o_ys = take(size_t(p.sh2.splits) * T * d->d * 4);
   }
+  // the one-launch decode layer's own region, last in the workspace.  For a size query it is the
+  // largest any T' <= min(T, 32) needs, so a workspace sized for T serves every smaller call
+  // (the regions before it only grow with T).
+  p.dec = plan_decode(d, std::min<int64_t>(T, 32), decode_warps());
+  if (p.dec.ok) {
+    size_t bytes = p.dec.bytes;
+    if (for_size)
+      for (int64_t t = 1; t < std::min<int64_t>(T, 32); ++t) bytes = std::max(bytes, plan_decode(d, t, decode_warps()).bytes);
+    p.o_dec = take(bytes);
+    if (T > 32) p.dec.ok = false;
+  }
   p.total = o;
   return p;
 }
+
+bool use_decode_launch(const LayerPlan &p) { return p.dec.ok && g_decode_mode.load(std::memory_order_relaxed) == 0; }
 
 // The shared expert reads only x, so it runs on a second stream beside the routed chain
 // (router, sort, two grouped GEMMs) and joins back before the combine: its 16-bit weight stream
@@ -232,12 +251,18 @@ extern "C" int moe_device_error(moe_stream_t stream, int32_t *host_code) {
   MOE_REQUIRE(host_code != nullptr, "host_code is NULL");
   int v = 0;
   MOE_TRY(read_device_error(reinterpret_cast<cudaStream_t>(stream), &v));
+  MOE_TRY(decode_error_take(&v));
   *host_code = v;
   return MOE_OK;
 }
 extern "C" int moe_version(void) { return 1; }
 
 extern "C" int moe_checked_build(void) { return MOE_CHECKED; }
+
+extern "C" int moe_set_decode_mode(int mode) {
+  MOE_REQUIRE(mode == 0 || mode == 1, "decode mode must be 0 (one launch) or 1 (kernel chain)");
+  return g_decode_mode.exchange(mode);
+}
 
 extern "C" int moe_check_status(moe_stream_t stream, int32_t *host_flags) {
   MOE_REQUIRE(host_flags != nullptr, "host_flags is NULL");
@@ -334,7 +359,7 @@ extern "C" int moe_shared_expert(const void *x, int x_dtype, const void *w_gate_
 
 extern "C" size_t moe_layer_workspace_size(const moe_layer_desc *desc, int64_t T) {
   if (check_desc(desc) != MOE_OK || T < 0) return 0;
-  return plan_layer(desc, T).total;
+  return plan_layer(desc, T, true).total;
 }
 
 extern "C" int moe_layer_routing_view(const moe_layer_desc *desc, int64_t T, void *workspace,
@@ -354,6 +379,7 @@ extern "C" int moe_layer_routing_view(const moe_layer_desc *desc, int64_t T, voi
 extern "C" int moe_layer_launch_count(const moe_layer_desc *desc, int64_t T) {
   if (check_desc(desc) != MOE_OK || T <= 0) return 0;
   const LayerPlan p = plan_layer(desc, T);
+  if (use_decode_launch(p)) return 1;
   int n = (desc->router_dtype == MOE_F32 ? 1 : 2) /*route*/ + permute_launches(p.R, desc->E) /*permute*/ + 1 /*fc1*/ + (p.fc1.partial ? 1 : 0) + 1 /*fc2*/ + (p.fused_combine ? 0 : 1) /*combine*/;
   if (desc->Fs > 0) n += 2 + (p.sh1.partial ? 1 : 0);
   return n;
@@ -394,6 +420,15 @@ extern "C" int moe_layer_forward_profiled(const moe_layer_desc *desc, const moe_
   const int64_t d = desc->d, F = desc->F, E = desc->E;
   const int k = desc->k;
   const int64_t F1 = desc->act == MOE_ACT_SWIGLU ? 2 * F : F;
+  if (!stage_events && use_decode_launch(p)) {
+    // one launch for the whole layer; its control words are cleared first, except inside a
+    // stream capture, where the launch relies on them being zero (every completed launch leaves
+    // them so; moe_layer_graph_create runs one call before it captures)
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return check_launch("layer: capture status");
+    return launch_decode_layer(desc, w, x, T, out, ids, gate, offs, perm, inv, h, ws + p.o_dec, p.dec,
+                               cs == cudaStreamCaptureStatusNone, st);
+  }
 
   auto mark = [&](int stage) -> int {
     if (!stage_events) return MOE_OK;

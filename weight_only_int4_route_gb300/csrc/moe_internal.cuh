@@ -150,6 +150,20 @@ bool tc_supported(const GemmArgs &g);
 bool tc_shape_ok(int64_t E, int64_t K, int64_t N, int bits, int group, int act);
 int launch_gemm_tc(const GemmArgs &g, cudaStream_t st);
 int read_device_error(cudaStream_t st, int *out);
+int decode_error_take(int *out);   // device error word of the one-launch decode layer
+
+// One-launch decode layer (decode_layer.cu): whether it takes a layer of T tokens, how the work
+// is cut, and the layout of its own region of the layer workspace.
+struct DecodePlan {
+  bool ok;
+  int NCR, S2, CH2, S3, CH3, rcmax, nts;
+  size_t o_rpart, o_ypart, o_hs, o_yspart, o_rctab, o_ctrl, bytes;   // offsets inside the region
+};
+DecodePlan plan_decode(const moe_layer_desc *ds, int64_t T, int64_t warps);
+int decode_warps();
+int launch_decode_layer(const moe_layer_desc *ds, const moe_layer_weights *w, const void *x, int64_t T, void *out,
+                        int32_t *ids, float *gate, int32_t *offs, int32_t *perm, int32_t *inv, void *h, char *fused,
+                        const DecodePlan &pl, bool zero_ctrl, cudaStream_t st);
 // Kernel launches of one moe_permute call for R rows over E experts.
 int permute_launches(int64_t R, int64_t E);
 // out[r, c] = act(sum_s part[s, r, c]) (SWIGLU pairs column c with c + N/2).
@@ -391,6 +405,71 @@ __device__ __forceinline__ bool offsets_usable(const int32_t *off, int E, int64_
   (void)off; (void)E; (void)R; (void)fail;
   return true;
 #endif
+}
+
+// Top-k + softmax for one token (one warp), E <= 256 logits in shared memory: the k largest
+// logits in descending order (equal logits: lower expert id first), gate = softmax over all E
+// logits taken at the chosen ids (divided by the k gates' sum when renorm != 0).  Lane j < k
+// writes ids[j] and gates[j].
+__device__ __forceinline__ void topk_softmax_warp(const float *logits, int E, int k, int renorm, int32_t *ids,
+                                  float *gates) {
+  const int lane = threadIdx.x & 31;
+  constexpr int kPer = 256 / 32;   // E <= 256
+  float v[kPer];
+  bool taken[kPer];
+  float mx = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = e < E ? logits[e] : -INFINITY;
+    taken[i] = e >= E;
+    mx = fmaxf(mx, v[i]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  float sum = 0.f;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i)
+    if (lane + 32 * i < E) sum += expf(v[i] - mx);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  float gsum = 0.f;
+  float my_gate = 0.f;  // lane j keeps gate j
+  int my_id = 0;
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int e = lane + 32 * i;
+      if (!taken[i] && (v[i] > bv || (v[i] == bv && e < bi))) {
+        bv = v[i];
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ov > bv || (ov == bv && oi < bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kPer; ++i)
+      if (lane + 32 * i == bi) taken[i] = true;
+    const float g = expf(bv - mx) / sum;
+    gsum += g;
+    if (lane == j) {
+      my_gate = g;
+      my_id = bi;
+    }
+  }
+  if (lane < k) {
+    ids[lane] = my_id;
+    gates[lane] = renorm ? my_gate / gsum : my_gate;
+  }
 }
 
 __device__ __forceinline__ void pdl_enter() {

@@ -16,71 +16,8 @@ namespace moe {
 namespace {
 
 constexpr int kTok = 16;     // tokens per CTA
-constexpr int kKC = 64;      // reduction chunk staged in shared memory
 constexpr int kMaxE = 256;
 constexpr int kThreads = 128;
-
-// Top-k + softmax for one token (one warp).  logits: E floats in shared memory.
-__device__ void topk_softmax_warp(const float *logits, int E, int k, int renorm, int32_t *ids,
-                                  float *gates) {
-  const int lane = threadIdx.x & 31;
-  constexpr int kPer = kMaxE / 32;
-  float v[kPer];
-  bool taken[kPer];
-  float mx = -INFINITY;
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const int e = lane + 32 * i;
-    v[i] = e < E ? logits[e] : -INFINITY;
-    taken[i] = e >= E;
-    mx = fmaxf(mx, v[i]);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  float sum = 0.f;
-#pragma unroll
-  for (int i = 0; i < kPer; ++i)
-    if (lane + 32 * i < E) sum += expf(v[i] - mx);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-  float gsum = 0.f;
-  float my_gate = 0.f;  // lane j keeps gate j
-  int my_id = 0;
-  for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      const int e = lane + 32 * i;
-      if (!taken[i] && (v[i] > bv || (v[i] == bv && e < bi))) {
-        bv = v[i];
-        bi = e;
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (ov > bv || (ov == bv && oi < bi)) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < kPer; ++i)
-      if (lane + 32 * i == bi) taken[i] = true;
-    const float g = expf(bv - mx) / sum;
-    gsum += g;
-    if (lane == j) {
-      my_gate = g;
-      my_id = bi;
-    }
-  }
-  if (lane < k) {
-    ids[lane] = my_id;
-    gates[lane] = renorm ? my_gate / gsum : my_gate;
-  }
-}
 
 // fp32 router weights: fp32 FMA logits (small routers).  CTA = kTok tokens; the (token,
 // expert) pairs are spread over the threads (expert fastest, so a warp reads consecutive

@@ -54,6 +54,7 @@ _SIGS = {
     "moe_version": (_c_int, []),
     "moe_device_error": (_c_int, [_vp, ctypes.POINTER(ctypes.c_int32)]),
     "moe_checked_build": (_c_int, []),
+    "moe_set_decode_mode": (_c_int, [_c_int]),
     "moe_check_status": (_c_int, [_vp, ctypes.POINTER(ctypes.c_int32)]),
     "moe_packed_size": (_c_size, [_c_i64, _c_i64, _c_i64, _c_int, _c_int]),
     "moe_packed_scale_offset": (_c_size, [_c_i64, _c_i64, _c_i64, _c_int]),
@@ -128,6 +129,15 @@ def lib_checked() -> ctypes.CDLL:
     if _lib_checked is None:
         _lib_checked = _load(LIB_CHECKED_PATH)
     return _lib_checked
+
+
+def set_decode_mode(mode: str) -> str:
+    """'launch' (a decode step as one kernel launch, the default) or 'chain' (the kernel chain);
+    returns the previous mode."""
+    prev = lib().moe_set_decode_mode({"launch": 0, "chain": 1}[mode])
+    if prev < 0:
+        _check(prev, "moe_set_decode_mode")
+    return {0: "launch", 1: "chain"}[prev]
 
 
 def check_status(device="cuda:0", L: Optional[ctypes.CDLL] = None) -> tuple[int, int]:
