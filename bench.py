@@ -63,7 +63,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="decode-sized steps: launch kernels one by one")
     ap.add_argument("--decode-chain", action="store_true",
-                    help="decode-sized steps: the chain of kernels instead of the one-launch layer")
+                    help="decode-sized steps: always the chain of kernels")
+    ap.add_argument("--decode-launch", action="store_true",
+                    help="decode-sized steps: always the one-launch layer kernel (where the layer allows it)")
     ap.add_argument("--elb", action="store_true",
                     help="time ELB counting + top-M for one chunk boundary instead of the layer (separate metric)")
     ap.add_argument("--codec", action="store_true",
@@ -195,6 +197,8 @@ def run_ours(args, cfg, T, n_layers, world, rank, local):
     torch.cuda.set_device(dev)
     if args.decode_chain:
         M.set_decode_mode("chain")
+    elif args.decode_launch:
+        M.set_decode_mode("launch")
     dist = None
     if world > 1:
         import torch.distributed as dist

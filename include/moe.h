@@ -295,16 +295,18 @@ int moe_layer_routing_view(const moe_layer_desc *desc, int64_t T, void *workspac
 /* Number of kernels one moe_layer_forward(desc, T tokens) enqueues (0 if invalid or T == 0). */
 int moe_layer_launch_count(const moe_layer_desc *desc, int64_t T);
 /* How moe_layer_forward runs a decode step.  [Specter] technical novelty and method step (5):
- * the draft runs all expert sub-computations of a step in one fused launch.  Mode 0 (the
- * default): a layer of T <= 32 tokens with 4-bit expert weights, E <= 256 and T*k <= 256 runs as
- * ONE kernel launch (router, top-k, sort, FC1 + activation, FC2, shared expert, combine; the
- * work units are ordered by their dependencies and waits between them are bounded), the same
- * arithmetic as the chain; its control words live in the layer workspace and are cleared by a
- * memset before the launch, except while `stream` is being captured (every completed launch
- * leaves them zero again; a capture must follow one uncaptured call on the same workspace, as
- * moe_layer_graph_create does; after moe_device_error reports a code, make one uncaptured call
- * before replaying a graph).  Mode 1: always the chain of kernels.  Process-wide; returns the
- * previous mode, or MOE_ERR_INVALID_ARG. */
+ * the draft runs all expert sub-computations of a step in one fused launch.  A layer of T <= 32
+ * tokens with 4-bit expert weights, E <= 256 and T*k <= 256 can run as ONE kernel launch (router,
+ * top-k, sort, FC1 + activation, FC2, shared expert, combine; work units ordered by their
+ * dependencies, every wait bounded), the same arithmetic as the chain of kernels; its control
+ * words live in the layer workspace and are cleared by a memset before the launch, except while
+ * `stream` is being captured (every completed launch leaves them zero again; a capture must follow
+ * one uncaptured call on the same workspace, as moe_layer_graph_create does; after
+ * moe_device_error reports a code, make one uncaptured call before replaying a graph).
+ * mode 0 (default): automatic -- one launch when the step streams at most 16 MB of expert and
+ * shared-expert weights (there launch and dependency latency dominate; measured on GB300), else
+ * the chain; mode 1: always the chain; mode 2: one launch whenever the layer allows it.
+ * Process-wide; returns the previous mode, or MOE_ERR_INVALID_ARG. */
 int moe_set_decode_mode(int mode);
 /* x: (T, d) dtype; out: (T, d) dtype.  With a shared expert (Fs > 0) the shared expert's kernels
  * run on a second stream owned by the library (one per calling thread and device, created on

@@ -1,4 +1,4 @@
-"""The decode step as one kernel launch (moe_set_decode_mode 0, the default for T <= 32).
+"""The decode step as one kernel launch (moe_set_decode_mode 2; automatic mode picks it for small steps).
 
 The single launch runs router, top-k, sort, FC1 + activation, FC2, the shared expert and the
 combine ("Specter" summary page, technical novelty: one launch for all expert sub-computations
@@ -23,7 +23,9 @@ def M():
     from weight_only_int4_route_gb300 import build, moe
     build.build()
     moe.lib()
-    return moe
+    prev = moe.set_decode_mode("launch")   # the one-launch kernel for every decode-sized step here
+    yield moe
+    moe.set_decode_mode(prev)
 
 
 def _layer(M, cfg, w, T):

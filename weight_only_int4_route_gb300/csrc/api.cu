@@ -5,6 +5,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <cmath>
 
 #include "moe_internal.cuh"
 
@@ -113,9 +114,15 @@ struct LayerPlan {
   size_t o_ids, o_gate, o_off, o_perm, o_inv, o_rws, o_pws, o_xp, o_p1, o_h, o_y, o_hs, o_ps1, o_ys, o_dec, total;
 };
 
-// 0: a decode step (T <= 32 on a supported layer) runs as one launch; 1: always the chain of
-// kernels (moe_set_decode_mode).
+// How a decode step runs (moe_set_decode_mode): 0 automatic, 1 always the chain of kernels,
+// 2 one launch whenever the layer allows it.
 std::atomic<int> g_decode_mode{0};
+// Automatic choice: one launch when the step streams at most this many weight bytes.  Measured
+// on GB300: a small layer (1 MB of expert weights, T = 16) takes 29 us as one launch and 42 us as
+// the chain (launch and dependency latency dominate), while from the Qwen-shaped T = 1 step
+// (88 MB) up the chain's many-warp weight-stream kernels stream faster than the one-launch
+// kernel's one block per SM (51 vs 48 us; Phi-shaped T = 16: 231 vs 168 us).
+constexpr double kDecodeLaunchMaxBytes = 16e6;
 
 int check_desc(const moe_layer_desc *d) {
   MOE_REQUIRE(d != nullptr, "desc is NULL");
@@ -181,7 +188,21 @@ LayerPlan plan_layer(const moe_layer_desc *d, int64_t T, bool for_size = false) 
   return p;
 }
 
-bool use_decode_launch(const LayerPlan &p) { return p.dec.ok && g_decode_mode.load(std::memory_order_relaxed) == 0; }
+// Expert and shared-expert weight bytes a step of T tokens streams (experts drawn uniformly).
+double decode_bytes(const moe_layer_desc *d, int64_t T) {
+  const double er = double(d->E), R = double(T * d->k);
+  const double active = std::min(er, std::max(1.0, er * (1.0 - std::pow(1.0 - 1.0 / er, R))));
+  const double F1 = d->act == MOE_ACT_SWIGLU ? 2.0 * d->F : double(d->F);
+  const double per_expert = (double(d->d) * F1 + double(d->F) * d->d) * d->bits / 8.0;
+  return active * per_expert + 3.0 * d->d * d->Fs * 2.0;
+}
+
+bool use_decode_launch(const moe_layer_desc *d, const LayerPlan &p) {
+  if (!p.dec.ok) return false;
+  const int mode = g_decode_mode.load(std::memory_order_relaxed);
+  if (mode == 1) return false;
+  return mode == 2 || decode_bytes(d, p.T) <= kDecodeLaunchMaxBytes;
+}
 
 // The shared expert reads only x, so it runs on a second stream beside the routed chain
 // (router, sort, two grouped GEMMs) and joins back before the combine: its 16-bit weight stream
@@ -260,7 +281,7 @@ extern "C" int moe_version(void) { return 1; }
 extern "C" int moe_checked_build(void) { return MOE_CHECKED; }
 
 extern "C" int moe_set_decode_mode(int mode) {
-  MOE_REQUIRE(mode == 0 || mode == 1, "decode mode must be 0 (one launch) or 1 (kernel chain)");
+  MOE_REQUIRE(mode >= 0 && mode <= 2, "decode mode must be 0 (automatic), 1 (kernel chain) or 2 (one launch)");
   return g_decode_mode.exchange(mode);
 }
 
@@ -379,7 +400,7 @@ extern "C" int moe_layer_routing_view(const moe_layer_desc *desc, int64_t T, voi
 extern "C" int moe_layer_launch_count(const moe_layer_desc *desc, int64_t T) {
   if (check_desc(desc) != MOE_OK || T <= 0) return 0;
   const LayerPlan p = plan_layer(desc, T);
-  if (use_decode_launch(p)) return 1;
+  if (use_decode_launch(desc, p)) return 1;
   int n = (desc->router_dtype == MOE_F32 ? 1 : 2) /*route*/ + permute_launches(p.R, desc->E) /*permute*/ + 1 /*fc1*/ + (p.fc1.partial ? 1 : 0) + 1 /*fc2*/ + (p.fused_combine ? 0 : 1) /*combine*/;
   if (desc->Fs > 0) n += 2 + (p.sh1.partial ? 1 : 0);
   return n;
@@ -420,7 +441,7 @@ extern "C" int moe_layer_forward_profiled(const moe_layer_desc *desc, const moe_
   const int64_t d = desc->d, F = desc->F, E = desc->E;
   const int k = desc->k;
   const int64_t F1 = desc->act == MOE_ACT_SWIGLU ? 2 * F : F;
-  if (!stage_events && use_decode_launch(p)) {
+  if (!stage_events && use_decode_launch(desc, p)) {
     // one launch for the whole layer; its control words are cleared first, except inside a
     // stream capture, where the launch relies on them being zero (every completed launch leaves
     // them so; moe_layer_graph_create runs one call before it captures)

@@ -131,13 +131,16 @@ def lib_checked() -> ctypes.CDLL:
     return _lib_checked
 
 
+_DECODE_MODES = {"auto": 0, "chain": 1, "launch": 2}
+
+
 def set_decode_mode(mode: str) -> str:
-    """'launch' (a decode step as one kernel launch, the default) or 'chain' (the kernel chain);
-    returns the previous mode."""
-    prev = lib().moe_set_decode_mode({"launch": 0, "chain": 1}[mode])
+    """'auto' (the default: one kernel launch for small decode steps, else the chain), 'chain' (the
+    kernel chain) or 'launch' (one launch whenever the layer allows it); returns the previous mode."""
+    prev = lib().moe_set_decode_mode(_DECODE_MODES[mode])
     if prev < 0:
         _check(prev, "moe_set_decode_mode")
-    return {0: "launch", 1: "chain"}[prev]
+    return {v: k for k, v in _DECODE_MODES.items()}[prev]
 
 
 def check_status(device="cuda:0", L: Optional[ctypes.CDLL] = None) -> tuple[int, int]:
