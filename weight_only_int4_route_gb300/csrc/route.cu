@@ -22,11 +22,20 @@ constexpr int kThreads = 128;
 // fp32 router weights: fp32 FMA logits (small routers).  CTA = kTok tokens; the (token,
 // expert) pairs are spread over the threads (expert fastest, so a warp reads consecutive
 // weights), and each reduction chunk of x and of the router weights is staged in shared memory
-// with coalesced loads; a chunk holds at most kWChunk weights, so few experts give long chunks.
+// with coalesced loads; a chunk holds at most kWChunk weights and kXW columns of x, so few
+// experts give long chunks.  Each thread issues its share of a chunk's loads kU at a time into
+// registers before storing any of them: a lone CTA (a decode step) would otherwise wait one
+// full memory latency per element it stages.  A thread owns NP (token, expert) pairs (NP =
+// ceil(kTok * E / kThreads), rounded up to a power of two) and steps through the chunk's
+// reduction index once, advancing all NP sums together: the NP independent FMA chains and the
+// unrolled shared-memory reads keep the pipeline full where one chain per pair at a time would
+// wait on every read.
 constexpr int kWChunk = 2048;
+constexpr int kXW = 256;
+constexpr int kU = 16;
 
-template <typename T>
-__global__ void __launch_bounds__(kThreads) route_f32_kernel(const T *__restrict__ x,
+template <typename T, int NP>
+__global__ void __launch_bounds__(kThreads, 1) route_f32_kernel(const T *__restrict__ x,
                                                               const float *__restrict__ wr,
                                                               const float *__restrict__ bias,
                                                               int T_, int d, int E, int k,
@@ -34,39 +43,63 @@ __global__ void __launch_bounds__(kThreads) route_f32_kernel(const T *__restrict
                                                               float *__restrict__ gates) {
   pdl_enter();   // see launch_pdl
   __shared__ float ws[kWChunk];
-  __shared__ float xs[kTok][kWChunk / 16];
+  __shared__ float xs[kTok][kXW + 1];   // +1: the rows of one warp's tokens fall in different banks
   __shared__ float lg[kTok][kMaxE + 1];
   const int tid = threadIdx.x, warp = tid >> 5;
   const int tok0 = blockIdx.x * kTok;
   // rows of Wr per chunk: as many as fit kWChunk weights, at most the xs width
-  const int rows = min(kWChunk / 16, kWChunk / E);
-  constexpr int kPairs = kTok * kMaxE / kThreads;
+  const int rows = min(kXW, kWChunk / E);
   const int npairs = kTok * E;
-  float acc[kPairs];
+  float acc[NP];
+  int xo[NP], eo[NP];   // the pair's x row offset and expert; pairs past npairs compute a dummy
 #pragma unroll
-  for (int i = 0; i < kPairs; ++i) acc[i] = 0.f;
+  for (int i = 0; i < NP; ++i) {
+    acc[i] = 0.f;
+    const int pidx = min(tid + i * kThreads, npairs - 1), r = pidx / E;
+    xo[i] = r * (kXW + 1);
+    eo[i] = pidx - r * E;
+  }
   for (int k0 = 0; k0 < d; k0 += rows) {
     const int kc = min(rows, d - k0);
-    for (int i = tid; i < kc * E; i += kThreads) ws[i] = wr[int64_t(k0) * E + i];
-    for (int i = tid; i < kTok * kc; i += kThreads) {
-      const int r = i / kc, c = i % kc;
-      xs[r][c] = tok0 + r < T_ ? to_f32(x[int64_t(tok0 + r) * d + k0 + c]) : 0.f;
+    const int nw = kc * E, nx = kTok * kc;
+    const float *wsrc = wr + int64_t(k0) * E;
+    for (int b = tid; b < nw; b += kThreads * kU) {
+      float v[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = b + u * kThreads;
+        v[u] = i < nw ? __ldg(wsrc + i) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = b + u * kThreads;
+        if (i < nw) ws[i] = v[u];
+      }
+    }
+    for (int b = tid; b < nx; b += kThreads * kU) {
+      float v[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = b + u * kThreads, r = i / kc, c = i - r * kc;
+        v[u] = (i < nx && tok0 + r < T_) ? to_f32(x[int64_t(tok0 + r) * d + k0 + c]) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = b + u * kThreads, r = i / kc;
+        if (i < nx) xs[r][i - r * kc] = v[u];
+      }
     }
     __syncthreads();
+    const float *xf = &xs[0][0];
+#pragma unroll 4
+    for (int c = 0; c < kc; ++c) {
 #pragma unroll
-    for (int i = 0; i < kPairs; ++i) {
-      const int pidx = tid + i * kThreads;
-      if (pidx < npairs) {
-        const int r = pidx / E, e = pidx - r * E;
-        float s = acc[i];
-        for (int c = 0; c < kc; ++c) s = fmaf(xs[r][c], ws[c * E + e], s);
-        acc[i] = s;
-      }
+      for (int i = 0; i < NP; ++i) acc[i] = fmaf(xf[xo[i] + c], ws[c * E + eo[i]], acc[i]);
     }
     __syncthreads();
   }
 #pragma unroll
-  for (int i = 0; i < kPairs; ++i) {
+  for (int i = 0; i < NP; ++i) {
     const int pidx = tid + i * kThreads;
     if (pidx < npairs) {
       const int r = pidx / E, e = pidx - r * E;
@@ -80,6 +113,22 @@ __global__ void __launch_bounds__(kThreads) route_f32_kernel(const T *__restrict
   }
 }
 
+
+// NP = the smallest power of two >= need_np (need_np <= kTok * kMaxE / kThreads = 32)
+template <typename T>
+void launch_route_f32(int need_np, unsigned grid, cudaStream_t st, const T *x, const float *wr, const float *bias,
+                      int T_, int d, int E, int k, int renorm, int32_t *ids, float *gates) {
+  auto go = [&](auto kern) {
+    launch_pdl(kern, dim3(grid), dim3(kThreads), 0, st, x, wr, bias, T_, d, E, k, renorm, ids, gates);
+  };
+  if (need_np <= 1) go(route_f32_kernel<T, 1>);
+  else if (need_np <= 2) go(route_f32_kernel<T, 2>);
+  else if (need_np <= 4) go(route_f32_kernel<T, 4>);
+  else if (need_np <= 8) go(route_f32_kernel<T, 8>);
+  else if (need_np <= 16) go(route_f32_kernel<T, 16>);
+  else go(route_f32_kernel<T, 32>);
+}
+static_assert(kTok * kMaxE / kThreads <= 32, "route_f32_kernel instances cover every E");
 
 // ---- split-K router: partial logits per (K split, token, expert), then a fixed-order reduce ----
 // CTA = 64 tokens (4 warps x m16) x one K range; the router weights are staged row-major with
@@ -302,12 +351,14 @@ extern "C" int moe_route_topk(const void *x, int x_dtype, const void *w_router, 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const unsigned grid = unsigned(cdiv(T, kTok));
   if (wr_dtype == MOE_F32) {
+    const int need_np = int(cdiv(int64_t(kTok) * E, kThreads));
     if (x_dtype == MOE_F16)
-      launch_pdl(route_f32_kernel<__half>, dim3(grid), dim3(kThreads), 0, st, static_cast<const __half *>(x),
-          static_cast<const float *>(w_router), bias, int(T), int(d), int(E), k, renormalize, ids, gate_w);
+      launch_route_f32<__half>(need_np, grid, st, static_cast<const __half *>(x), static_cast<const float *>(w_router),
+                               bias, int(T), int(d), int(E), k, renormalize, ids, gate_w);
     else
-      launch_pdl(route_f32_kernel<__nv_bfloat16>, dim3(grid), dim3(kThreads), 0, st, static_cast<const __nv_bfloat16 *>(x),
-          static_cast<const float *>(w_router), bias, int(T), int(d), int(E), k, renormalize, ids, gate_w);
+      launch_route_f32<__nv_bfloat16>(need_np, grid, st, static_cast<const __nv_bfloat16 *>(x),
+                                      static_cast<const float *>(w_router), bias, int(T), int(d), int(E), k,
+                                      renormalize, ids, gate_w);
   } else {
     const size_t need = moe_route_topk_workspace_size(T, d, E);
     MOE_REQUIRE(workspace && aligned16(workspace), "workspace must be non-null and 16-byte aligned");
