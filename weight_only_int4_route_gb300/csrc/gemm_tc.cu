@@ -87,11 +87,17 @@ constexpr long long kTimeoutCycles = 4000000000LL;  // ~2 s at 2 GHz
 
 enum : int { kErrTimeoutFull = 1, kErrTimeoutFree = 2, kErrTimeoutReady = 3, kErrTimeoutD = 4, kErrTimeoutDrain = 5 };
 
-// 4/8-bit: packed words (SWIZZLE_NONE boxes), dequantized into TMEM.  16-bit: the weights are
+// 4/8-bit: packed words, dequantized into TMEM.  A stage holds 128 channel rows of kRowBytes
+// (64 B INT4, 128 B INT8), copied with the swizzle of that width, so 16-byte piece j of row r
+// sits at piece j ^ ((r * kRowBytes / 128) & (kRowBytes / 16 - 1)): the dequant warps (lane =
+// row) read a piece of eight consecutive rows per quarter-warp without bank conflicts, where the
+// plain layout put 4 (INT4) or 8 (INT8) of them on the same banks.  16-bit: the weights are
 // the A operand as they are, TMA-loaded with the same 128-byte swizzle as the activations and
 // read by the MMA from shared memory (no dequant work); a stage is then 64 KB, so three stages.
 template <int BITS> struct WB {
   static constexpr int kWordsPerRow = kBK * BITS / 32;    // u32 words per channel per stage
+  static constexpr int kRowBytes = kWordsPerRow * 4;
+  static constexpr int kSwzMask = kRowBytes / 16 - 1;
   static constexpr int kBytes = kBM * kWordsPerRow * 4;   // weight stage bytes
   static constexpr int kStages = BITS == 16 ? 3 : kStagesQ;
 };
@@ -117,10 +123,13 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *b) {
 __device__ __forceinline__ void mbar_expect_tx(uint64_t *b, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(su32(b)), "r"(bytes) : "memory");
 }
+// A waiting thread is suspended in hardware until the phase completes (or the hint, 1 ms, runs
+// out) instead of re-issuing the test: the compute warps waiting on their stages would otherwise
+// take issue slots from the single-thread MMA and copy loops on their SM sub-partitions.
 __device__ __forceinline__ bool mbar_try(uint64_t *b, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 1000000;\n selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
       : "r"(su32(b)), "r"(parity)
       : "memory");
@@ -132,7 +141,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity, volatile
   const long long t0 = clock64();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try(b, parity)) return true;
-    if ((it & 63) == 0) {
+    if ((it & 7) == 0) {
       if (*abort_flag) return false;
       if (clock64() - t0 > kTimeoutCycles) {
         *abort_flag = 1;
@@ -167,15 +176,6 @@ __device__ __forceinline__ void tc_commit(uint64_t *bar) {
                : "memory");
 }
 
-__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                          uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 // A from shared memory (16-bit weights)
 __device__ __forceinline__ void tc_mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                           uint32_t accumulate) {
@@ -183,6 +183,30 @@ __device__ __forceinline__ void tc_mma_ss(uint32_t d_tmem, uint64_t a_desc, uint
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// The eight MMAs of one 128-wide K block (A from tensor memory), in one statement: the first
+// accumulates only when `acc` is set, the others always; MMA j reads A columns a + 8j and the
+// B descriptor advanced by j's start offset (16-byte units: 2 per 16-wide step inside a 64-wide
+// swizzle atom column, half16 to the next column block).  The offsets are added to the low word
+// only: the start-address field cannot carry (shared addresses stay below 256 KB).
+template <int HALF16>
+__device__ __forceinline__ void tc_mma_kblock_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  const uint32_t bl = uint32_t(b), bh = uint32_t(b >> 32);
+  asm volatile(
+      "{\n .reg .pred p, t;\n .reg .b32 a1, bl1;\n .reg .b64 bd;\n"
+      " setp.ne.b32 p, %5, 0;\n setp.eq.b32 t, %5, %5;\n"
+      " mov.b64 bd, {%2, %3};\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, p;\n"
+      " add.u32 a1, %1, 8;\n add.u32 bl1, %2, 2;\n mov.b64 bd, {bl1, %3};\n tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], bd, %4, t;\n"
+      " add.u32 a1, %1, 16;\n add.u32 bl1, %2, 4;\n mov.b64 bd, {bl1, %3};\n tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], bd, %4, t;\n"
+      " add.u32 a1, %1, 24;\n add.u32 bl1, %2, 6;\n mov.b64 bd, {bl1, %3};\n tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], bd, %4, t;\n"
+      " add.u32 a1, %1, 32;\n add.u32 bl1, %2, %6;\n mov.b64 bd, {bl1, %3};\n tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], bd, %4, t;\n"
+      " add.u32 a1, %1, 40;\n add.u32 bl1, %2, %7;\n mov.b64 bd, {bl1, %3};\n tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], bd, %4, t;\n"
+      " add.u32 a1, %1, 48;\n add.u32 bl1, %2, %8;\n mov.b64 bd, {bl1, %3};\n tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], bd, %4, t;\n"
+      " add.u32 a1, %1, 56;\n add.u32 bl1, %2, %9;\n mov.b64 bd, {bl1, %3};\n tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], bd, %4, t;\n"
+      "}\n" ::"r"(d), "r"(a), "r"(bl), "r"(bh), "r"(idesc), "r"(acc), "n"(HALF16), "n"(HALF16 + 2), "n"(HALF16 + 4),
+      "n"(HALF16 + 6)
       : "memory");
 }
 
@@ -495,11 +519,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t bd0 = sw128_desc(su32(sB + s * kBBytes));
           const uint32_t a_col = tmem + kACol0 + uint32_t(s) * kAStageCols;
           const uint64_t ad0 = BITS == 16 ? sw128_desc(su32(sW + s * kWBytes)) : 0;
+          if constexpr (BITS == 16) {
 #pragma unroll
-          for (int j = 0; j < kBK / 16; ++j) {
-            const uint64_t off = uint64_t(((j >> 2) * kBHalf + (j & 3) * 32) >> 4);
-            if constexpr (BITS == 16) tc_mma_ss(d_tmem, ad0 + off, bd0 + off, idesc, (kb | j) != 0);
-            else tc_mma_ts(d_tmem, a_col + uint32_t(j * 8), bd0 + off, idesc, (kb | j) != 0);
+            for (int j = 0; j < kBK / 16; ++j) {
+              const uint64_t off = uint64_t(((j >> 2) * kBHalf + (j & 3) * 32) >> 4);
+              tc_mma_ss(d_tmem, ad0 + off, bd0 + off, idesc, (kb | j) != 0);
+            }
+          } else {
+            static_assert(kBK == 128, "tc_mma_kblock_ts issues the eight MMAs of a 128-wide K block");
+            tc_mma_kblock_ts<kBHalf / 16>(d_tmem, a_col, bd0, idesc, uint32_t(kb));
           }
           tc_commit(&freeb[s]);
         }
@@ -539,45 +567,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint8_t *wp = sW + s * kWBytes + r * (kWords * 4);
+        const int swz = ((r * WB<BITS>::kRowBytes) >> 7) & WB<BITS>::kSwzMask;   // this row's piece swizzle
         const uint32_t ta = tmem + (uint32_t(q * 32) << 16) + kACol0 + uint32_t(s) * kAStageCols;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {   // two 64-wide halves of the K block, 32 columns each
-          uint32_t pr[32];
-          if constexpr (BITS != 8) {   // 4-bit (16-bit never reaches the dequant warps)
-            const uint4 w0 = *reinterpret_cast<const uint4 *>(wp + 32 * h);
-            const uint4 w1 = *reinterpret_cast<const uint4 *>(wp + 32 * h + 16);
-            const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+        for (int c = 0; c < 4; ++c) {   // 32-wide quarters of the K block: 16 columns of pairs each
+          uint32_t pr[16];
+          if constexpr (BITS != 8) {   // 4-bit (16-bit never reaches the dequant warps): one piece
+            const uint4 w = *reinterpret_cast<const uint4 *>(wp + 16 * (c ^ swz));
+            const uint32_t words[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
+            for (int i = 0; i < 4; ++i) {
               uint32_t hh[4];
               i2f_int4(words[i], hh, T());
 #pragma unroll
               for (int j = 0; j < 4; ++j) pr[4 * i + j] = hh[j];
             }
-          } else {
-            uint32_t words[16];
+          } else {                     // 8-bit: two pieces
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              const uint4 w = *reinterpret_cast<const uint4 *>(wp + 64 * h + 16 * v);
-              words[4 * v] = w.x;
-              words[4 * v + 1] = w.y;
-              words[4 * v + 2] = w.z;
-              words[4 * v + 3] = w.w;
-            }
+            for (int v = 0; v < 2; ++v) {
+              const uint4 w = *reinterpret_cast<const uint4 *>(wp + 16 * ((2 * c + v) ^ swz));
+              const uint32_t words[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              uint32_t hh[2];
-              i2f_int8(words[i], hh, T());
-              pr[2 * i] = hh[0];
-              pr[2 * i + 1] = hh[1];
+              for (int i = 0; i < 4; ++i) {
+                uint32_t hh[2];
+                i2f_int8(words[i], hh, T());
+                pr[8 * v + 2 * i] = hh[0];
+                pr[8 * v + 2 * i + 1] = hh[1];
+              }
             }
           }
           if (p.group != 0) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) pr[j] = scale_pair(pr[j], s2, T());
+            for (int j = 0; j < 16; ++j) pr[j] = scale_pair(pr[j], s2, T());
           }
-          tc_st16(ta + uint32_t(32 * h), *reinterpret_cast<const uint32_t(*)[16]>(&pr[0]));
-          tc_st16(ta + uint32_t(32 * h + 16), *reinterpret_cast<const uint32_t(*)[16]>(&pr[16]));
+          tc_st16(ta + uint32_t(16 * c), pr);
         }
         tc_wait_st();
         tc_fence_before();
@@ -677,7 +700,9 @@ int launch_typed(const GemmArgs &g, cudaStream_t st) {
     const cuuint32_t box[2] = {cuuint32_t(WB<BITS>::kWordsPerRow), cuuint32_t(kBM / 2)};
     const cuuint32_t es[2] = {1, 1};
     const CUresult r = enc(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void *>(g.w), dims, strides, box, es,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           WB<BITS>::kRowBytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return set_error(MOE_ERR_CUDA, "weight tensor map encode failed (%d)", int(r));
   }

@@ -19,116 +19,176 @@ constexpr int kTok = 16;     // tokens per CTA
 constexpr int kMaxE = 256;
 constexpr int kThreads = 128;
 
-// fp32 router weights: fp32 FMA logits (small routers).  CTA = kTok tokens; the (token,
-// expert) pairs are spread over the threads (expert fastest, so a warp reads consecutive
-// weights), and each reduction chunk of x and of the router weights is staged in shared memory
-// with coalesced loads; a chunk holds at most kWChunk weights and kXW columns of x, so few
-// experts give long chunks.  Each thread issues its share of a chunk's loads kU at a time into
-// registers before storing any of them: a lone CTA (a decode step) would otherwise wait one
-// full memory latency per element it stages.  A thread owns NP (token, expert) pairs (NP =
-// ceil(kTok * E / kThreads), rounded up to a power of two) and steps through the chunk's
-// reduction index once, advancing all NP sums together: the NP independent FMA chains and the
-// unrolled shared-memory reads keep the pipeline full where one chain per pair at a time would
-// wait on every read.
+// fp32 router weights: fp32 FMA logits (small routers).  CTA = kTok tokens, kF32Threads
+// threads; the (token, expert) pairs are spread over the threads (expert fastest, so a warp reads
+// consecutive weights).  The reduction runs over chunks of at most kXW columns of x and kWChunk
+// router weights (so few experts give long chunks), staged in shared memory.  With d % 8 == 0
+// the staging loads are 16-byte vectors, every one of a chunk issued before any is stored, and
+// the next chunk's loads are issued before the current chunk is multiplied (register double
+// buffer), so a lone CTA (a decode step) waits on memory about once per launch rather than once
+// per chunk; other d take the same route with scalar loads.  A thread owns NP (token, expert)
+// pairs (NP = ceil(kTok * E / kF32Threads), rounded up to a power of two) and steps through the
+// chunk's reduction index once, advancing all NP sums together.  The top-k and softmax run one
+// warp per token (two tokens per warp).
+constexpr int kF32Threads = 256;
 constexpr int kWChunk = 2048;
 constexpr int kXW = 256;
-constexpr int kU = 16;
+constexpr int kWV = kWChunk / 4 / kF32Threads;           // float4 weight pieces per thread per chunk
+constexpr int kXV = kTok * kXW / 8 / kF32Threads;        // 16-byte activation pieces per thread per chunk
+constexpr int kSU = 8;                                   // scalar path: loads in flight per thread
 
-template <typename T, int NP>
-__global__ void __launch_bounds__(kThreads, 1) route_f32_kernel(const T *__restrict__ x,
-                                                              const float *__restrict__ wr,
-                                                              const float *__restrict__ bias,
-                                                              int T_, int d, int E, int k,
-                                                              int renorm, int32_t *__restrict__ ids,
-                                                              float *__restrict__ gates) {
+template <typename T, int NP, bool VEC>
+__global__ void __launch_bounds__(kF32Threads, 1) route_f32_kernel(const T *__restrict__ x,
+                                                                 const float *__restrict__ wr,
+                                                                 const float *__restrict__ bias,
+                                                                 int T_, int d, int E, int k,
+                                                                 int renorm, int32_t *__restrict__ ids,
+                                                                 float *__restrict__ gates) {
   pdl_enter();   // see launch_pdl
-  __shared__ float ws[kWChunk];
+  __shared__ __align__(16) float ws[kWChunk];
   __shared__ float xs[kTok][kXW + 1];   // +1: the rows of one warp's tokens fall in different banks
   __shared__ float lg[kTok][kMaxE + 1];
   const int tid = threadIdx.x, warp = tid >> 5;
   const int tok0 = blockIdx.x * kTok;
-  // rows of Wr per chunk: as many as fit kWChunk weights, at most the xs width
-  const int rows = min(kXW, kWChunk / E);
+  // columns per chunk: as many as fit kWChunk weights, at most kXW, a multiple of 8
+  const int rows = min(kXW, (kWChunk / E) & ~7);
   const int npairs = kTok * E;
   float acc[NP];
   int xo[NP], eo[NP];   // the pair's x row offset and expert; pairs past npairs compute a dummy
 #pragma unroll
   for (int i = 0; i < NP; ++i) {
     acc[i] = 0.f;
-    const int pidx = min(tid + i * kThreads, npairs - 1), r = pidx / E;
+    const int pidx = min(tid + i * kF32Threads, npairs - 1), r = pidx / E;
     xo[i] = r * (kXW + 1);
     eo[i] = pidx - r * E;
   }
-  for (int k0 = 0; k0 < d; k0 += rows) {
-    const int kc = min(rows, d - k0);
-    const int nw = kc * E, nx = kTok * kc;
-    const float *wsrc = wr + int64_t(k0) * E;
-    for (int b = tid; b < nw; b += kThreads * kU) {
-      float v[kU];
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int i = b + u * kThreads;
-        v[u] = i < nw ? __ldg(wsrc + i) : 0.f;
-      }
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int i = b + u * kThreads;
-        if (i < nw) ws[i] = v[u];
-      }
-    }
-    for (int b = tid; b < nx; b += kThreads * kU) {
-      float v[kU];
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int i = b + u * kThreads, r = i / kc, c = i - r * kc;
-        v[u] = (i < nx && tok0 + r < T_) ? to_f32(x[int64_t(tok0 + r) * d + k0 + c]) : 0.f;
-      }
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int i = b + u * kThreads, r = i / kc;
-        if (i < nx) xs[r][i - r * kc] = v[u];
-      }
-    }
-    __syncthreads();
-    const float *xf = &xs[0][0];
+  const float *xf = &xs[0][0];
+  auto multiply = [&](int kc) {
 #pragma unroll 4
     for (int c = 0; c < kc; ++c) {
 #pragma unroll
       for (int i = 0; i < NP; ++i) acc[i] = fmaf(xf[xo[i] + c], ws[c * E + eo[i]], acc[i]);
     }
-    __syncthreads();
+  };
+  if constexpr (VEC) {
+    // piece q of a chunk: weights q < nw / 4 (float4), activations: row q / (kc / 8), 8 columns
+    float4 wv[kWV];
+    uint4 xv[kXV];
+    auto load = [&](int k0) {
+      const int kc = min(rows, d - k0), nw4 = kc * E / 4, nx8 = kTok * (kc / 8);
+      const float4 *wsrc = reinterpret_cast<const float4 *>(wr + int64_t(k0) * E);
+#pragma unroll
+      for (int u = 0; u < kWV; ++u) {
+        const int q = tid + u * kF32Threads;
+        if (q < nw4) wv[u] = __ldg(wsrc + q);
+      }
+#pragma unroll
+      for (int u = 0; u < kXV; ++u) {
+        const int q = tid + u * kF32Threads, r = q / (kc / 8), c8 = q - r * (kc / 8);
+        xv[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (q < nx8 && tok0 + r < T_)
+          xv[u] = __ldg(reinterpret_cast<const uint4 *>(x + int64_t(tok0 + r) * d + k0) + c8);
+      }
+    };
+    auto store = [&](int k0) {
+      const int kc = min(rows, d - k0), nw4 = kc * E / 4, nx8 = kTok * (kc / 8);
+#pragma unroll
+      for (int u = 0; u < kWV; ++u) {
+        const int q = tid + u * kF32Threads;
+        if (q < nw4) reinterpret_cast<float4 *>(ws)[q] = wv[u];
+      }
+#pragma unroll
+      for (int u = 0; u < kXV; ++u) {
+        const int q = tid + u * kF32Threads, r = q / (kc / 8), c8 = q - r * (kc / 8);
+        if (q < nx8) {
+          const T *h = reinterpret_cast<const T *>(&xv[u]);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) xs[r][8 * c8 + j] = to_f32(h[j]);
+        }
+      }
+    };
+    load(0);
+    for (int k0 = 0; k0 < d; k0 += rows) {
+      store(k0);
+      __syncthreads();
+      if (k0 + rows < d) load(k0 + rows);   // next chunk in flight while this one is multiplied
+      multiply(min(rows, d - k0));
+      __syncthreads();
+    }
+  } else {
+    for (int k0 = 0; k0 < d; k0 += rows) {
+      const int kc = min(rows, d - k0);
+      const int nw = kc * E, nx = kTok * kc;
+      const float *wsrc = wr + int64_t(k0) * E;
+      for (int b = tid; b < nw; b += kF32Threads * kSU) {
+        float v[kSU];
+#pragma unroll
+        for (int u = 0; u < kSU; ++u) {
+          const int i = b + u * kF32Threads;
+          v[u] = i < nw ? __ldg(wsrc + i) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < kSU; ++u) {
+          const int i = b + u * kF32Threads;
+          if (i < nw) ws[i] = v[u];
+        }
+      }
+      for (int b = tid; b < nx; b += kF32Threads * kSU) {
+        float v[kSU];
+#pragma unroll
+        for (int u = 0; u < kSU; ++u) {
+          const int i = b + u * kF32Threads, r = i / kc, c = i - r * kc;
+          v[u] = (i < nx && tok0 + r < T_) ? to_f32(x[int64_t(tok0 + r) * d + k0 + c]) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < kSU; ++u) {
+          const int i = b + u * kF32Threads, r = i / kc;
+          if (i < nx) xs[r][i - r * kc] = v[u];
+        }
+      }
+      __syncthreads();
+      multiply(kc);
+      __syncthreads();
+    }
   }
 #pragma unroll
   for (int i = 0; i < NP; ++i) {
-    const int pidx = tid + i * kThreads;
+    const int pidx = tid + i * kF32Threads;
     if (pidx < npairs) {
       const int r = pidx / E, e = pidx - r * E;
       lg[r][e] = acc[i] + (bias ? bias[e] : 0.f);
     }
   }
   __syncthreads();
-  for (int r = warp; r < kTok; r += kThreads / 32) {
+  for (int r = warp; r < kTok; r += kF32Threads / 32) {
     const int tok = tok0 + r;
     if (tok < T_) topk_softmax_warp(lg[r], E, k, renorm, ids + int64_t(tok) * k, gates + int64_t(tok) * k);
   }
 }
 
 
-// NP = the smallest power of two >= need_np (need_np <= kTok * kMaxE / kThreads = 32)
-template <typename T>
-void launch_route_f32(int need_np, unsigned grid, cudaStream_t st, const T *x, const float *wr, const float *bias,
-                      int T_, int d, int E, int k, int renorm, int32_t *ids, float *gates) {
+// NP = the smallest power of two >= need_np (need_np <= kTok * kMaxE / kF32Threads = 16)
+template <typename T, bool VEC>
+void launch_route_f32_v(int need_np, unsigned grid, cudaStream_t st, const T *x, const float *wr, const float *bias,
+                        int T_, int d, int E, int k, int renorm, int32_t *ids, float *gates) {
   auto go = [&](auto kern) {
-    launch_pdl(kern, dim3(grid), dim3(kThreads), 0, st, x, wr, bias, T_, d, E, k, renorm, ids, gates);
+    launch_pdl(kern, dim3(grid), dim3(kF32Threads), 0, st, x, wr, bias, T_, d, E, k, renorm, ids, gates);
   };
-  if (need_np <= 1) go(route_f32_kernel<T, 1>);
-  else if (need_np <= 2) go(route_f32_kernel<T, 2>);
-  else if (need_np <= 4) go(route_f32_kernel<T, 4>);
-  else if (need_np <= 8) go(route_f32_kernel<T, 8>);
-  else if (need_np <= 16) go(route_f32_kernel<T, 16>);
-  else go(route_f32_kernel<T, 32>);
+  if (need_np <= 1) go(route_f32_kernel<T, 1, VEC>);
+  else if (need_np <= 2) go(route_f32_kernel<T, 2, VEC>);
+  else if (need_np <= 4) go(route_f32_kernel<T, 4, VEC>);
+  else if (need_np <= 8) go(route_f32_kernel<T, 8, VEC>);
+  else go(route_f32_kernel<T, 16, VEC>);
 }
-static_assert(kTok * kMaxE / kThreads <= 32, "route_f32_kernel instances cover every E");
+template <typename T>
+void launch_route_f32(unsigned grid, cudaStream_t st, const T *x, const float *wr, const float *bias, int T_, int d,
+                      int E, int k, int renorm, int32_t *ids, float *gates) {
+  const int need_np = int(cdiv(int64_t(kTok) * E, kF32Threads));
+  if (d % 8 == 0) launch_route_f32_v<T, true>(need_np, grid, st, x, wr, bias, T_, d, E, k, renorm, ids, gates);
+  else launch_route_f32_v<T, false>(need_np, grid, st, x, wr, bias, T_, d, E, k, renorm, ids, gates);
+}
+static_assert(kTok * kMaxE / kF32Threads <= 16, "route_f32_kernel instances cover every E");
+static_assert(kWChunk % (4 * kF32Threads) == 0 && (kTok * kXW) % (8 * kF32Threads) == 0, "staging pieces");
 
 // ---- split-K router: partial logits per (K split, token, expert), then a fixed-order reduce ----
 // CTA = 64 tokens (4 warps x m16) x one K range; the router weights are staged row-major with
@@ -351,12 +411,11 @@ extern "C" int moe_route_topk(const void *x, int x_dtype, const void *w_router, 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const unsigned grid = unsigned(cdiv(T, kTok));
   if (wr_dtype == MOE_F32) {
-    const int need_np = int(cdiv(int64_t(kTok) * E, kThreads));
     if (x_dtype == MOE_F16)
-      launch_route_f32<__half>(need_np, grid, st, static_cast<const __half *>(x), static_cast<const float *>(w_router),
-                               bias, int(T), int(d), int(E), k, renormalize, ids, gate_w);
+      launch_route_f32<__half>(grid, st, static_cast<const __half *>(x), static_cast<const float *>(w_router), bias,
+                               int(T), int(d), int(E), k, renormalize, ids, gate_w);
     else
-      launch_route_f32<__nv_bfloat16>(need_np, grid, st, static_cast<const __nv_bfloat16 *>(x),
+      launch_route_f32<__nv_bfloat16>(grid, st, static_cast<const __nv_bfloat16 *>(x),
                                       static_cast<const float *>(w_router), bias, int(T), int(d), int(E), k,
                                       renormalize, ids, gate_w);
   } else {
