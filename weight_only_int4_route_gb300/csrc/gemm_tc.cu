@@ -18,22 +18,29 @@
 // Warp roles (one CTA per SM, persistent over tiles):
 //   warps 0-7    epilogue: warp w reads TMEM lanes 32*(w%4).. and every other 32-column chunk
 //                of the tile's columns; scale / activation, global stores;
-//   warp 8       producer: TMA of the packed weight block and the activation block;
+//   warp 8       activation copies: TMA of the tile's activation block into the activation ring;
 //   warp 9       MMA issuer (one thread);
 //   warps 10-21  dequant, three groups of four warps; group g converts the K blocks with
-//                index = g (mod 3), so each pipeline stage always belongs to the same group.
-//                Warp w owns TMEM lanes 32*(w%4).. (one output channel per lane); it reads
-//                that channel's packed words from shared memory, converts them with the
-//                magic-number I2F (and the group-128 scale) and stores the 16-bit pairs into
-//                the A stage.
+//                index = g (mod 3), so each weight stage and each A stage always belongs to the
+//                same group.  Warp w owns TMEM lanes 32*(w%4).. (one output channel per lane);
+//                it reads that channel's packed words from shared memory, converts them with
+//                the magic-number I2F (and the group-128 scale) and stores the 16-bit pairs into
+//                the A stage;
+//   warp 22      weight copies: TMA of the packed weight block into the weight ring, and a
+//                rolling L2 prefetch of the weight blocks ahead of them.
 // Tiles are 128 output channels x up to 160 routed rows (an expert with up to 160 rows is one
 // tile).  TMEM columns: [0,320) two 160-column accumulators, [320,512) three 64-column A stages.
 //
-// Synchronisation per 128-wide K block: the producer's TMA completes `full`; the dequant
-// group waits on it, fills the TMEM A stage and arrives on `ready`; the MMA thread waits
-// only on `ready` (the data behind it was seen complete by the dequant warps) and issues
-// eight MMAs; one commit on `free` releases both the shared-memory stage and the A stage.
-// A K block of 128 keeps 512 tensor cycles of work queued behind each wait/commit pair.
+// Synchronisation per 128-wide K block (stage s = block index mod 3 in every ring): the weight
+// copy completes `wfull[s]`; the dequant group waits on it and on `sfree[s]` (the MMAs that last
+// read the A stage are done), fills the A stage, releases the weight stage (`wfree[s]`), waits
+// for the block's activation copy (`bfull[s]`) and arrives on `ready[s]`; the MMA thread waits on
+// `ready[s]` alone, issues eight MMAs and commits once to `sfree[s]`, which frees the activation
+// stage and the A stage.  Weights and activations travel in separate rings with their own copy
+// warps, so a block's dequant starts when its weights land, not when its (five times larger)
+// activation block does, and the single MMA thread does one wait and one commit per block.
+// A K block of 128 keeps 512-640 tensor cycles of work queued behind each wait/commit pair.
+// (16-bit weights: no dequant; the MMA thread waits on both copies and `sfree` frees both stages.)
 //
 // Every wait on an mbarrier is bounded (about two seconds); on expiry the CTA records an
 // error code in a device word, stops issuing work, drains its own asynchronous copies and
@@ -57,17 +64,18 @@ namespace {
 constexpr int kEpiWarps = 8;        // epilogue warps (two per TMEM lane quarter)
 constexpr int kDqGroups = 3;        // dequant warp groups (each: 4 warps covering 128 lanes)
 constexpr int kProdWarp = kEpiWarps, kMmaWarp = kEpiWarps + 1, kDqWarp0 = kEpiWarps + 2;
-constexpr int kThreads = (kDqWarp0 + 4 * kDqGroups) * 32;
+constexpr int kWProdWarp = kDqWarp0 + 4 * kDqGroups;   // weight copies and their L2 prefetch
+constexpr int kThreads = (kWProdWarp + 1) * 32;
 constexpr int kBM = 128;          // output channels per tile (MMA M)
 constexpr int kBNMax = 160;       // rows per tile at most (MMA N upper bound)
 constexpr int kBK = 128;          // K per pipeline stage
-constexpr int kStagesQ = 3;       // pipeline stages (shared memory and TMEM A), quantized weights
-// Every fill of a stage must go to the same dequant group.  A group waits on full[s] by phase
-// parity, which cannot tell "one phase ahead" from "complete": with groups taking K blocks
-// round-robin over a stage count they do not divide, the group of fill it + kStages could reach
-// full[s] while fill it (another group's) was still in flight -- TMA completions of different
-// stages are not ordered -- and pass the wait at once.
-static_assert(kStagesQ % kDqGroups == 0, "each stage must belong to one dequant group");
+constexpr int kAStages = 3;       // TMEM A stages (quantized weights), one per dequant group
+// Every fill of a weight stage or an A stage must go to the same dequant group.  A group waits on
+// its stage's barriers by phase parity, which cannot tell "one phase ahead" from "complete":
+// with groups taking K blocks round-robin over a stage count they do not divide, the group of
+// fill it + kStages could reach the barrier while fill it (another group's) was still in flight
+// -- TMA completions of different stages are not ordered -- and pass the wait at once.
+static_assert(kAStages % kDqGroups == 0, "each A stage must belong to one dequant group");
 static_assert(kBNMax % 32 == 0 && kBNMax <= 256, "tile rows: whole 32-column epilogue chunks, MMA N <= 256");
 constexpr int kMaxE = 256;
 constexpr uint32_t kTmemCols = 512;
@@ -81,7 +89,7 @@ template <int BITS> struct TB {
   static constexpr int kBBytes = 2 * kBHalf;              // activation stage
   static constexpr uint32_t kACol0 = 2 * kBN;             // A stages after the two accumulators
 };
-static_assert(2 * kBNMax + kStagesQ * 64 <= 512, "tensor memory: accumulators + A stages");
+static_assert(2 * kBNMax + kAStages * 64 <= 512, "tensor memory: accumulators + A stages");
 constexpr uint32_t kAStageCols = kBK / 2;    // 64 columns of 16-bit pairs
 constexpr long long kTimeoutCycles = 4000000000LL;  // ~2 s at 2 GHz
 
@@ -99,8 +107,14 @@ template <int BITS> struct WB {
   static constexpr int kRowBytes = kWordsPerRow * 4;
   static constexpr int kSwzMask = kRowBytes / 16 - 1;
   static constexpr int kBytes = kBM * kWordsPerRow * 4;   // weight stage bytes
-  static constexpr int kStages = BITS == 16 ? 3 : kStagesQ;
+  // weight and activation rings have as many stages as there are A stages, so stage s of every
+  // ring holds the same K block and one MMA commit frees all three
+  static constexpr int kWStages = kAStages;
+  static constexpr int kBStages = kAStages;
 };
+static_assert(WB<4>::kWStages % kDqGroups == 0 && WB<8>::kWStages % kDqGroups == 0, "weight stages per group");
+static_assert(WB<4>::kRowBytes == 64 && WB<8>::kRowBytes == 128 && WB<16>::kSwzMask == 15,
+              "swizzled weight rows: 64-byte (INT4) and 128-byte (INT8) copies");
 
 struct TcParams {
   const int32_t *offsets;
@@ -361,17 +375,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_enter();   // see launch_pdl
   constexpr int kWBytes = WB<BITS>::kBytes;
   constexpr int kWords = WB<BITS>::kWordsPerRow;
-  constexpr int kStages = WB<BITS>::kStages;
+  constexpr int kWS = WB<BITS>::kWStages, kBS = WB<BITS>::kBStages;
   constexpr int kBN = TB<BITS>::kBN, kBHalf = TB<BITS>::kBHalf, kBBytes = TB<BITS>::kBBytes;
   constexpr uint32_t kACol0 = TB<BITS>::kACol0;
   extern __shared__ __align__(1024) uint8_t dsmem[];
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dsmem) + 1023) & ~uintptr_t(1023));
-  uint8_t *sB = base;                                   // kStages x kBBytes (two 1024-aligned K halves)
-  uint8_t *sW = sB + kStages * kBBytes;                 // kStages x kWBytes
-  float *sX = reinterpret_cast<float *>(sW + kStages * kWBytes);  // SwiGLU exchange: 2 halves x 32 x 64 fp32
+  uint8_t *sB = base;                                   // kBS x kBBytes (two 1024-aligned K halves)
+  uint8_t *sW = sB + kBS * kBBytes;                     // kWS x kWBytes
+  float *sX = reinterpret_cast<float *>(sW + kWS * kWBytes);  // SwiGLU exchange: 2 halves x 32 x 64 fp32
   uint64_t *bar = reinterpret_cast<uint64_t *>(sX + 2 * 32 * 64);
-  uint64_t *full = bar, *ready = bar + kStages, *freeb = bar + 2 * kStages;
-  uint64_t *d_full = bar + 3 * kStages, *d_empty = d_full + 2, *drain = d_empty + 2;
+  // wfull/wfree: weight ring; bfull: activation ring; ready: TMEM A stages; sfree: the MMAs of
+  // stage s are done (frees the activation stage, the A stage and, for 16-bit weights, the weight
+  // stage)
+  static_assert(kWS == kAStages && kBS == kAStages, "one stage index for every ring");
+  uint64_t *wfull = bar, *wfree = wfull + kWS, *bfull = wfree + kWS, *ready = bfull + kBS, *sfree = ready + kAStages;
+  uint64_t *d_full = sfree + kAStages, *d_empty = d_full + 2, *drain = d_empty + 2;
   int *s_tstart = reinterpret_cast<int *>(drain + 1);
   int *s_off = s_tstart + kMaxE + 1;
   int *scratch = s_off + kMaxE + 1;
@@ -383,10 +401,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- setup: barriers, TMEM, tile table
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
+    for (int s = 0; s < kAStages; ++s) {
+      mbar_init(&wfull[s], 1);
+      mbar_init(&wfree[s], 4);   // the dequant group's 4 warps (quantized weights)
+      mbar_init(&bfull[s], 1);
       mbar_init(&ready[s], 4);
-      mbar_init(&freeb[s], 1);
+      mbar_init(&sfree[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&d_full[s], 1);
@@ -419,9 +439,39 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const int nkb = p.K / kBK;
   const int is_bf16 = std::is_same<T, __nv_bfloat16>::value ? 1 : 0;
+  // the drain of a copy ring: every issued fill has landed before the CTA may exit (2 bits per
+  // stage: 0 = never filled, else the parity of its last fill + 1)
+  auto drain_ring = [&](uint64_t *fullb, int nst, uint32_t issued) {
+    for (int s = 0; s < nst; ++s)
+      if ((issued >> (2 * s)) & 3u) {
+        volatile int never = 0;
+        mbar_wait(&fullb[s], ((issued >> (2 * s)) & 3u) - 1, &never, kErrTimeoutDrain);
+      }
+  };
 
   if (warp == kProdWarp) {
-    // ------------------------------------------------ producer (TMA)
+    // ------------------------------------------------ activation copies (TMA)
+    if (lane == 0) {
+      uint32_t it = 0, issued = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+        const Tile t = decode_tile(tile, s_tstart, s_off, E, p.ncb, kBN);
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = it % kBS;
+          if (!mbar_wait(&sfree[s], ((it / kBS) & 1) ^ 1, abort_flag, kErrTimeoutFree)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(&bfull[s], kBBytes);
+          tma_load_2d(sB + s * kBBytes, &map_x, kb * kBK, t.row0, &bfull[s]);
+          tma_load_2d(sB + s * kBBytes + kBHalf, &map_x, kb * kBK + 64, t.row0, &bfull[s]);
+          issued = (issued & ~(3u << (2 * s))) | ((((it / kBS) & 1) + 1) << (2 * s));
+        }
+      }
+      drain_ring(bfull, kBS, issued);
+    }
+  } else if (warp == kWProdWarp) {
+    // ------------------------------------------------ weight copies (TMA) + L2 prefetch
     if (lane == 0) {
       // rolling L2 prefetch of the weight blocks kPrefetch K blocks ahead of the stage copies (into
       // the CTA's next tile), so a stage copy waits on L2 rather than DRAM
@@ -452,45 +502,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       if (pf_tile < total_tiles) pf_rows();
       for (int i = 0; i < kPrefetch; ++i) pf_step();
-      uint32_t it = 0;
-      int issued[kStages];
-#pragma unroll
-      for (int s = 0; s < kStages; ++s) issued[s] = 0;
+      uint32_t it = 0, issued = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
         const Tile t = decode_tile(tile, s_tstart, s_off, E, p.ncb, kBN);
         const int rowA = t.e * p.N + (p.swiglu ? t.cb * (kBM / 2) : t.cb * kBM);
         const int rowB = p.swiglu ? t.e * p.N + (p.N >> 1) + t.cb * (kBM / 2) : rowA + kBM / 2;
         for (int kb = 0; kb < nkb; ++kb, ++it) {
-          const int s = it % kStages;
-          if (!mbar_wait(&freeb[s], ((it / kStages) & 1) ^ 1, abort_flag, kErrTimeoutFree)) {
+          const int s = it % kWS;
+          if (!mbar_wait(BITS == 16 ? &sfree[s] : &wfree[s], ((it / kWS) & 1) ^ 1, abort_flag, kErrTimeoutFree)) {
             ok = false;
             break;
           }
-          mbar_expect_tx(&full[s], kBBytes + kWBytes);
-          tma_load_2d(sB + s * kBBytes, &map_x, kb * kBK, t.row0, &full[s]);
-          tma_load_2d(sB + s * kBBytes + kBHalf, &map_x, kb * kBK + 64, t.row0, &full[s]);
+          mbar_expect_tx(&wfull[s], kWBytes);
           if constexpr (BITS == 16) {   // K halves of 16 KB; rows 0-63 (rowA..) then 64-127 (rowB..)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-              tma_load_2d(sW + s * kWBytes + h * kBHalf, &map_w, kb * kBK + 64 * h, rowA, &full[s]);
-              tma_load_2d(sW + s * kWBytes + h * kBHalf + kBHalf / 2, &map_w, kb * kBK + 64 * h, rowB, &full[s]);
+              tma_load_2d(sW + s * kWBytes + h * kBHalf, &map_w, kb * kBK + 64 * h, rowA, &wfull[s]);
+              tma_load_2d(sW + s * kWBytes + h * kBHalf + kBHalf / 2, &map_w, kb * kBK + 64 * h, rowB, &wfull[s]);
             }
           } else {
-            tma_load_2d(sW + s * kWBytes, &map_w, kb * kWords, rowA, &full[s]);
-            tma_load_2d(sW + s * kWBytes + kWBytes / 2, &map_w, kb * kWords, rowB, &full[s]);
+            tma_load_2d(sW + s * kWBytes, &map_w, kb * kWords, rowA, &wfull[s]);
+            tma_load_2d(sW + s * kWBytes + kWBytes / 2, &map_w, kb * kWords, rowB, &wfull[s]);
           }
-          issued[s] = int((it / kStages) & 1) + 1;  // parity of this fill, +1
+          issued = (issued & ~(3u << (2 * s))) | ((((it / kWS) & 1) + 1) << (2 * s));
           pf_step();
         }
       }
-      // drain: every issued copy has landed before the CTA may exit
-#pragma unroll
-      for (int s = 0; s < kStages; ++s)
-        if (issued[s]) {
-          volatile int never = 0;
-          mbar_wait(&full[s], uint32_t(issued[s] - 1), &never, kErrTimeoutDrain);
-        }
+      drain_ring(wfull, kWS, issued);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------ MMA issuer
@@ -506,20 +545,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem + uint32_t(db * kBN);
         for (int kb = 0; kb < nkb; ++kb, ++it) {
-          const int s = it % kStages;
-          // 16-bit weights are MMA-ready once the copies land; else the dequant group signals
-          if (!(BITS == 16 ? mbar_wait(&full[s], (it / kStages) & 1, abort_flag, kErrTimeoutFull)
-                           : mbar_wait(&ready[s], (it / kStages) & 1, abort_flag, kErrTimeoutReady))) {
+          const int s = it % kAStages;
+          const uint32_t par = (it / kAStages) & 1;
+          // 16-bit weights: both copies landed; quantized: the dequant group signals `ready` once
+          // its A stage is filled and it has seen the block's activation copy land
+          if (!(BITS == 16 ? mbar_wait(&wfull[s], par, abort_flag, kErrTimeoutFull) &&
+                                 mbar_wait(&bfull[s], par, abort_flag, kErrTimeoutFull)
+                           : mbar_wait(&ready[s], par, abort_flag, kErrTimeoutReady))) {
             ok = false;
             break;
           }
           tc_fence_after();
-          // descriptor of the stage built once; MMA j adds its start offset (16-byte units, no
-          // carry out of the 14-bit field: shared addresses stay below 256 KB)
           const uint64_t bd0 = sw128_desc(su32(sB + s * kBBytes));
-          const uint32_t a_col = tmem + kACol0 + uint32_t(s) * kAStageCols;
-          const uint64_t ad0 = BITS == 16 ? sw128_desc(su32(sW + s * kWBytes)) : 0;
           if constexpr (BITS == 16) {
+            // descriptor of the stage built once; MMA j adds its start offset (16-byte units, no
+            // carry out of the 14-bit field: shared addresses stay below 256 KB)
+            const uint64_t ad0 = sw128_desc(su32(sW + s * kWBytes));
 #pragma unroll
             for (int j = 0; j < kBK / 16; ++j) {
               const uint64_t off = uint64_t(((j >> 2) * kBHalf + (j & 3) * 32) >> 4);
@@ -527,9 +568,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           } else {
             static_assert(kBK == 128, "tc_mma_kblock_ts issues the eight MMAs of a 128-wide K block");
-            tc_mma_kblock_ts<kBHalf / 16>(d_tmem, a_col, bd0, idesc, uint32_t(kb));
+            tc_mma_kblock_ts<kBHalf / 16>(d_tmem, tmem + kACol0 + uint32_t(s) * kAStageCols, bd0, idesc, uint32_t(kb));
           }
-          tc_commit(&freeb[s]);
+          tc_commit(&sfree[s]);
         }
         if (ok) tc_commit(&d_full[db]);
       }
@@ -544,6 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;                  // TMEM lane quarter
     const int grp = (warp - kDqWarp0) >> 2;  // converts K blocks kb with kb % kDqGroups == grp
     const int r = q * 32 + lane;             // A row (channel within the tile)
+    const int swz = ((r * WB<BITS>::kRowBytes) >> 7) & WB<BITS>::kSwzMask;   // this row's piece swizzle
     uint32_t it = 0;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
@@ -555,20 +597,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint16_t *srow = p.scales + int64_t(t.e) * G * p.N + ch;
       for (int kb = 0; kb < nkb; ++kb, ++it) {
         if ((it % kDqGroups) != uint32_t(grp)) continue;
-        const int s = it % kStages;
+        const int sw = it % kWS, sa = it % kAStages;   // the same index: every ring has kAStages stages
         uint32_t s2 = 0;
         if (p.group != 0) {  // one scale per 128-wide K block (group 128)
           const uint16_t sb = srow[int64_t((kb * kBK) / p.group) * p.N];
           s2 = uint32_t(sb) | (uint32_t(sb) << 16);
         }
-        if (!mbar_wait(&full[s], (it / kStages) & 1, abort_flag, kErrTimeoutFull)) {
+        // the block's weights have landed, and the MMAs that read this A stage last are done
+        if (!mbar_wait(&wfull[sw], (it / kWS) & 1, abort_flag, kErrTimeoutFull) ||
+            !mbar_wait(&sfree[sa], ((it / kAStages) & 1) ^ 1, abort_flag, kErrTimeoutFree)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint8_t *wp = sW + s * kWBytes + r * (kWords * 4);
-        const int swz = ((r * WB<BITS>::kRowBytes) >> 7) & WB<BITS>::kSwzMask;   // this row's piece swizzle
-        const uint32_t ta = tmem + (uint32_t(q * 32) << 16) + kACol0 + uint32_t(s) * kAStageCols;
+        const uint8_t *wp = sW + sw * kWBytes + r * (kWords * 4);
+        const uint32_t ta = tmem + (uint32_t(q * 32) << 16) + kACol0 + uint32_t(sa) * kAStageCols;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {   // 32-wide quarters of the K block: 16 columns of pairs each
           uint32_t pr[16];
@@ -602,10 +645,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_st16(ta + uint32_t(16 * c), pr);
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&wfree[sw]);   // the block's weights are in registers / TMEM now
         tc_wait_st();
         tc_fence_before();
+        // the MMA thread waits on `ready` alone: the group also waits for the block's activation copy
+        if (!mbar_wait(&bfull[sa], (it / kAStages) & 1, abort_flag, kErrTimeoutFull)) {
+          ok = false;
+          break;
+        }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&ready[s]);
+        if (lane == 0) mbar_arrive(&ready[sa]);
       }
     }
     }
@@ -663,11 +713,24 @@ EncodeTiledFn encode_fn() {
 
 size_t smem_bytes(int bits) {
   const size_t wbytes = bits == 4 ? WB<4>::kBytes : (bits == 8 ? WB<8>::kBytes : WB<16>::kBytes);
-  const int st = bits == 16 ? WB<16>::kStages : kStagesQ;
+  const int ws = bits == 4 ? WB<4>::kWStages : (bits == 8 ? WB<8>::kWStages : WB<16>::kWStages);
+  const int bs = bits == 4 ? WB<4>::kBStages : (bits == 8 ? WB<8>::kBStages : WB<16>::kBStages);
   const size_t bbytes = bits == 16 ? TB<16>::kBBytes : TB<4>::kBBytes;
-  return 1024 /*align slack*/ + st * (bbytes + wbytes) + 2 * 32 * 64 * 4 + (3 * st + 5) * 8 +
+  return 1024 /*align slack*/ + bs * bbytes + ws * wbytes + 2 * 32 * 64 * 4 + (2 * ws + 2 * bs + 2 * kAStages + 5) * 8 +
          (2 * (kMaxE + 1) + 32 + 2) * 4;
 }
+static_assert(1024 + WB<4>::kBStages * TB<4>::kBBytes + WB<4>::kWStages * WB<4>::kBytes + 2 * 32 * 64 * 4 +
+                      (2 * WB<4>::kWStages + 2 * WB<4>::kBStages + 2 * kAStages + 5) * 8 + (2 * (kMaxE + 1) + 34) * 4 <=
+                  232448,
+              "INT4 shared memory");
+static_assert(1024 + WB<8>::kBStages * TB<8>::kBBytes + WB<8>::kWStages * WB<8>::kBytes + 2 * 32 * 64 * 4 +
+                      (2 * WB<8>::kWStages + 2 * WB<8>::kBStages + 2 * kAStages + 5) * 8 + (2 * (kMaxE + 1) + 34) * 4 <=
+                  232448,
+              "INT8 shared memory");
+static_assert(1024 + WB<16>::kBStages * TB<16>::kBBytes + WB<16>::kWStages * WB<16>::kBytes + 2 * 32 * 64 * 4 +
+                      (2 * WB<16>::kWStages + 2 * WB<16>::kBStages + 2 * kAStages + 5) * 8 + (2 * (kMaxE + 1) + 34) * 4 <=
+                  232448,
+              "16-bit shared memory");
 
 template <typename T, int BITS>
 int launch_typed(const GemmArgs &g, cudaStream_t st) {
