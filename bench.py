@@ -411,9 +411,6 @@ def run_ours(args, cfg, T, n_layers, world, rank, local):
 # An entry is valid only for the kernel version it was taken on: it is removed whenever that
 # kernel changes.
 MEASURED_TRAFFIC = {
-    ("encdec_int4", 3840, "fc1"): 75_372_032 + 5_958_400,
-    ("encdec_int4", 3840, "fc2"): 98_761_984 + 3_501_312,
-    ("phi", 8192, "fc1"): 568_060_928 + 197_525_504,
 }
 
 
