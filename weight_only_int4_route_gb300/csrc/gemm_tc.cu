@@ -116,6 +116,13 @@ static_assert(WB<4>::kWStages % kDqGroups == 0 && WB<8>::kWStages % kDqGroups ==
 static_assert(WB<4>::kRowBytes == 64 && WB<8>::kRowBytes == 128 && WB<16>::kSwzMask == 15,
               "swizzled weight rows: 64-byte (INT4) and 128-byte (INT8) copies");
 
+// Activation tensor maps with boxes of 32, 64, ... kBNMax rows: a tile copies the smallest box
+// that covers its rows, so an expert's last, partial tile does not pull up to 128 rows of the
+// next expert through shared memory (the MMA, sized to the tile's rows, never reads them).
+struct XMaps {
+  CUtensorMap box[kBNMax / 32];
+};
+
 struct TcParams {
   const int32_t *offsets;
   const uint16_t *scales;
@@ -370,7 +377,7 @@ __device__ __forceinline__ void epilogue_cols(const TcParams &p, const Tile &t, 
 
 template <typename T, int BITS>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
+    gemm_tc_kernel(const __grid_constant__ XMaps maps_x, const __grid_constant__ CUtensorMap map_w,
                    const TcParams p) {
   pdl_enter();   // see launch_pdl
   constexpr int kWBytes = WB<BITS>::kBytes;
@@ -462,9 +469,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          mbar_expect_tx(&bfull[s], kBBytes);
-          tma_load_2d(sB + s * kBBytes, &map_x, kb * kBK, t.row0, &bfull[s]);
-          tma_load_2d(sB + s * kBBytes + kBHalf, &map_x, kb * kBK + 64, t.row0, &bfull[s]);
+          const int nb = (t.nrows + 31) >> 5;            // 32-row units of the tile's box
+          const CUtensorMap *mx = &maps_x.box[nb - 1];
+          mbar_expect_tx(&bfull[s], uint32_t(nb) * 32 * 128 * 2);
+          tma_load_2d(sB + s * kBBytes, mx, kb * kBK, t.row0, &bfull[s]);
+          tma_load_2d(sB + s * kBBytes + kBHalf, mx, kb * kBK + 64, t.row0, &bfull[s]);
           issued = (issued & ~(3u << (2 * s))) | ((((it / kBS) & 1) + 1) << (2 * s));
         }
       }
@@ -736,13 +745,14 @@ template <typename T, int BITS>
 int launch_typed(const GemmArgs &g, cudaStream_t st) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return set_error(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-  CUtensorMap mx, mw;
-  {
+  XMaps mx{};
+  CUtensorMap mw;
+  for (int i = 0; i < TB<BITS>::kBN / 32; ++i) {   // box i: 64 columns (one 128-byte swizzle atom) x 32 (i + 1) rows
     const cuuint64_t dims[2] = {cuuint64_t(g.K), cuuint64_t(g.R)};
     const cuuint64_t strides[1] = {cuuint64_t(g.K) * 2};
-    const cuuint32_t box[2] = {64u, cuuint32_t(TB<BITS>::kBN)};  // one 128-byte swizzle atom column block
+    const cuuint32_t box[2] = {64u, cuuint32_t(32 * (i + 1))};
     const cuuint32_t es[2] = {1, 1};
-    const CUresult r = enc(&mx, std::is_same<T, __half>::value ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+    const CUresult r = enc(&mx.box[i], std::is_same<T, __half>::value ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                            2, const_cast<void *>(g.a), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return set_error(MOE_ERR_CUDA, "activation tensor map encode failed (%d)", int(r));
