@@ -411,6 +411,9 @@ def run_ours(args, cfg, T, n_layers, world, rank, local):
 # An entry is valid only for the kernel version it was taken on: it is removed whenever that
 # kernel changes.
 MEASURED_TRAFFIC = {
+    ("phi", 8192, "fc1"): 567_240_704 + 197_445_632,
+    ("encdec_int4", 3840, "fc1"): 75_360_256 + 5_082_624,
+    ("encdec_int4", 3840, "fc2"): 98_776_064 + 3_428_864,
 }
 
 
