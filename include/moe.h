@@ -188,9 +188,9 @@ int moe_permute(const int32_t *ids, const void *x, int x_dtype, int64_t T, int64
  * RN(q * s) in the operand dtype, as Algorithm 1 states. */
 /* Which kernel a grouped GEMM with these arguments (offsets given) runs, judged from the
  * average rows per active expert a = ceil(R / min(E, R)): 2 = the decode weight-stream kernel
- * (a <= 16); 1 = the tcgen05 tensor-memory kernel (a >= 17 for 4- and 8-bit weights, a >= 64
- * for 16-bit weights, when the shape suits it: K % 128 == 0, N % 128 == 0, or for SWIGLU
- * (N/2) % 64 == 0); 0 = the warp-MMA tile kernel (the rest). */
+ * (a <= 16); 1 = the tcgen05 tensor-memory kernel (a >= 17, when the shape suits it:
+ * K % 128 == 0, N % 128 == 0, or for SWIGLU (N/2) % 64 == 0); 0 = the warp-MMA tile kernel
+ * (the rest). */
 int moe_gemm_path(int64_t R, int64_t E, int64_t K, int64_t N, int bits, int group, int act);
 size_t moe_grouped_gemm_workspace_size(int64_t R, int64_t E, int64_t K, int64_t N, int bits,
                                        int act);

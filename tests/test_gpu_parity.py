@@ -289,7 +289,7 @@ def test_gemm_config_shapes_vs_oracle(M, name, which, counts):
 def test_shared_expert_vs_oracle(M):
     cfg = synth.CONFIGS["qwen"]
     w = synth.layer_weights(cfg)
-    for T in (1, 8, 100, 700):
+    for T in (1, 8, 17, 32, 63, 100, 700):   # gemv up to 16 rows, tcgen05 from 17
         x = synth.activations(cfg, T)
         gu = M.pack_weights(w.ws_gu.to(DEV)[None], None, 16, 0)
         dn = M.pack_weights(w.ws_d.to(DEV)[None], None, 16, 0)

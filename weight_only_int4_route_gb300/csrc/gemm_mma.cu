@@ -42,7 +42,8 @@ constexpr int kRowBytes = kKC * 2 + 32;
 constexpr int kMaxE = 256;
 constexpr int kEpStride = kNB + 8;  // fp32 epilogue tile row stride
 constexpr int kTcMinRows = 17;      // rows per active expert from which the tcgen05 path is used
-constexpr int kTcMinRows16 = 64;    // the same for 16-bit weights
+constexpr int kTcMinRows16 = 17;    // the same for 16-bit weights (measured: 17-63 rows of the
+                                    // Qwen-shaped shared expert take 42 us there, 63-80 us here)
 constexpr int kGemvMaxRows = 16;    // rows per active expert up to which the decode stream kernel is used
 
 template <int BITS> struct WT {
@@ -349,8 +350,6 @@ GemmPlan plan_gemm(int64_t R, int64_t E, int64_t K, int64_t N, int bits, int act
   const int64_t target = 2 * int64_t(num_sms());
   // the tcgen05 kernel takes these whole, without split-K (group is not known here: group 128 is
   // the only grouped size the API accepts, and the kernel takes it)
-  // (16-bit weights, twice the bytes per FLOP of INT8, stream better through the warp-MMA kernel
-  // up to 64 rows)
   const bool tc_rows = avg >= (bits == 16 ? kTcMinRows16 : kTcMinRows) && tc_shape_ok(E, K, N, bits, 0, act);
   while (!tc_rows && S * 2 <= std::max<int64_t>(1, nck / 2) && tiles * ncb_fused * S < target) S *= 2;
   const int64_t cps = cdiv(nck, S);
