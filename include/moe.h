@@ -308,6 +308,14 @@ int moe_layer_launch_count(const moe_layer_desc *desc, int64_t T);
  * the chain; mode 1: always the chain; mode 2: one launch whenever the layer allows it.
  * Process-wide; returns the previous mode, or MOE_ERR_INVALID_ARG. */
 int moe_set_decode_mode(int mode);
+/* The quantized tcgen05 GEMM runs as CTA pairs (clusters of two CTAs, tcgen05 cta_group::2,
+ * M = 256: each SM copies half of a tile's activation rows) when the output channels come in
+ * blocks of 256 (SWIGLU: 128 gate + 128 up) and the device can place the pairs, else on single
+ * CTAs (M = 128): the same arithmetic in the same order (bit-identical results).  Process-wide,
+ * default 0 (single CTAs: on GB300 the pairs measured slower, Phi-shaped FC1 1.73 against
+ * 1.27 ms, because every K block's readiness has to cross to the other CTA); returns the
+ * previous setting, or MOE_ERR_INVALID_ARG. */
+int moe_set_gemm_pairs(int on);
 /* x: (T, d) dtype; out: (T, d) dtype.  With a shared expert (Fs > 0) the shared expert's kernels
  * run on a second stream owned by the library (one per calling thread and device, created on
  * first use), forked from `stream` before the router and joined back into `stream` before the

@@ -285,6 +285,11 @@ extern "C" int moe_set_decode_mode(int mode) {
   return g_decode_mode.exchange(mode);
 }
 
+extern "C" int moe_set_gemm_pairs(int on) {
+  MOE_REQUIRE(on == 0 || on == 1, "on must be 0 or 1");
+  return set_gemm_pairs(on);
+}
+
 extern "C" int moe_check_status(moe_stream_t stream, int32_t *host_flags) {
   MOE_REQUIRE(host_flags != nullptr, "host_flags is NULL");
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)

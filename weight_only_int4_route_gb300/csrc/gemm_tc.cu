@@ -57,6 +57,14 @@ namespace moe {
 
 __device__ int g_moe_device_error = 0;
 
+// CTA pairs for the quantized GEMM (moe_set_gemm_pairs); off by default: measured on GB300 the
+// pairs are correct (bit-identical to single CTAs) but slower -- Phi FC1 1.73 vs 1.27 ms, encdec
+// FC1 64 vs 52 us -- because each K block's readiness must cross to the other CTA (about
+// 1-2 k cycles through the relay), more than the three A stages can hide
+std::atomic<bool> g_tc_pairs{false};
+
+int set_gemm_pairs(int on) { return g_tc_pairs.exchange(on != 0) ? 1 : 0; }
+
 MOE_DEFINE_CHECK_WORD(gemm_tc)
 
 namespace {
@@ -147,21 +155,31 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *b, uint32_t bytes) {
 // A waiting thread is suspended in hardware until the phase completes (or the hint, 1 ms, runs
 // out) instead of re-issuing the test: the compute warps waiting on their stages would otherwise
 // take issue slots from the single-thread MMA and copy loops on their SM sub-partitions.
+template <bool CL = false>
 __device__ __forceinline__ bool mbar_try(uint64_t *b, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 1000000;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(su32(b)), "r"(parity)
-      : "memory");
+  if constexpr (CL)   // barriers the other CTA of a pair arrives on (remote arrivals, multicast commits)
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, 1000000;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(su32(b)), "r"(parity)
+        : "memory");
+  else
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 1000000;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(su32(b)), "r"(parity)
+        : "memory");
   return ok != 0;
 }
 // Bounded wait: false if the CTA aborted or this wait expired (then the abort flag is set).
+template <bool CL = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity, volatile int *abort_flag, int code) {
-  if (mbar_try(b, parity)) return true;
+  if (mbar_try<CL>(b, parity)) return true;
   const long long t0 = clock64();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try(b, parity)) return true;
+    if (mbar_try<CL>(b, parity)) return true;
     if ((it & 7) == 0) {
       if (*abort_flag) return false;
       if (clock64() - t0 > kTimeoutCycles) {
@@ -171,6 +189,26 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity, volatile
       }
     }
   }
+}
+
+// ---- CTA pairs (clusters of two): addresses in the peer CTA, remote arrivals, cluster barrier
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+  return r;
+}
+// shared::cluster address of the same shared-memory location in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t map_to_rank(const void *p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(su32(p)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }
 
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
@@ -196,6 +234,19 @@ __device__ __forceinline__ void tc_commit(uint64_t *bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(su32(bar))
                : "memory");
 }
+// pairs: completion of the pair's MMAs issued so far, signalled on `bar` in both CTAs / in this one
+__device__ __forceinline__ void tc_commit_pair(uint64_t *bar) {
+  const uint16_t both = 3;
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n" ::"r"(
+          su32(bar)),
+      "h"(both)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit_pair_local(uint64_t *bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(su32(bar))
+               : "memory");
+}
 
 // A from shared memory (16-bit weights)
 __device__ __forceinline__ void tc_mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
@@ -212,25 +263,35 @@ __device__ __forceinline__ void tc_mma_ss(uint32_t d_tmem, uint64_t a_desc, uint
 // B descriptor advanced by j's start offset (16-byte units: 2 per 16-wide step inside a 64-wide
 // swizzle atom column, half16 to the next column block).  The offsets are added to the low word
 // only: the start-address field cannot carry (shared addresses stay below 256 KB).
-template <int HALF16>
+#define MOE_TC_MMA_KBLOCK(GROUP)                                                                                  \
+  asm volatile(                                                                                                   \
+      "{\n .reg .pred p, t;\n .reg .b32 a1, bl1;\n .reg .b64 bd;\n"                                            \
+      " setp.ne.b32 p, %5, 0;\n setp.eq.b32 t, %5, %5;\n"                                                       \
+      " mov.b64 bd, {%2, %3};\n tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], [%1], bd, %4, p;\n"             \
+      " add.u32 a1, %1, 8;\n add.u32 bl1, %2, 2;\n mov.b64 bd, {bl1, %3};\n"                                  \
+      " tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], [a1], bd, %4, t;\n"                                     \
+      " add.u32 a1, %1, 16;\n add.u32 bl1, %2, 4;\n mov.b64 bd, {bl1, %3};\n"                                 \
+      " tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], [a1], bd, %4, t;\n"                                     \
+      " add.u32 a1, %1, 24;\n add.u32 bl1, %2, 6;\n mov.b64 bd, {bl1, %3};\n"                                 \
+      " tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], [a1], bd, %4, t;\n"                                     \
+      " add.u32 a1, %1, 32;\n add.u32 bl1, %2, %6;\n mov.b64 bd, {bl1, %3};\n"                                \
+      " tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], [a1], bd, %4, t;\n"                                     \
+      " add.u32 a1, %1, 40;\n add.u32 bl1, %2, %7;\n mov.b64 bd, {bl1, %3};\n"                                \
+      " tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], [a1], bd, %4, t;\n"                                     \
+      " add.u32 a1, %1, 48;\n add.u32 bl1, %2, %8;\n mov.b64 bd, {bl1, %3};\n"                                \
+      " tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], [a1], bd, %4, t;\n"                                     \
+      " add.u32 a1, %1, 56;\n add.u32 bl1, %2, %9;\n mov.b64 bd, {bl1, %3};\n"                                \
+      " tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], [a1], bd, %4, t;\n"                                     \
+      "}\n" ::"r"(d), "r"(a), "r"(bl), "r"(bh), "r"(idesc), "r"(acc), "n"(HALF16), "n"(HALF16 + 2), "n"(HALF16 + 4), \
+      "n"(HALF16 + 6)                                                                                             \
+      : "memory")
+template <int HALF16, bool PAIR>
 __device__ __forceinline__ void tc_mma_kblock_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
   const uint32_t bl = uint32_t(b), bh = uint32_t(b >> 32);
-  asm volatile(
-      "{\n .reg .pred p, t;\n .reg .b32 a1, bl1;\n .reg .b64 bd;\n"
-      " setp.ne.b32 p, %5, 0;\n setp.eq.b32 t, %5, %5;\n"
-      " mov.b64 bd, {%2, %3};\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, p;\n"
-      " add.u32 a1, %1, 8;\n add.u32 bl1, %2, 2;\n mov.b64 bd, {bl1, %3};\n tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], bd, %4, t;\n"
-      " add.u32 a1, %1, 16;\n add.u32 bl1, %2, 4;\n mov.b64 bd, {bl1, %3};\n tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], bd, %4, t;\n"
-      " add.u32 a1, %1, 24;\n add.u32 bl1, %2, 6;\n mov.b64 bd, {bl1, %3};\n tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], bd, %4, t;\n"
-      " add.u32 a1, %1, 32;\n add.u32 bl1, %2, %6;\n mov.b64 bd, {bl1, %3};\n tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], bd, %4, t;\n"
-      " add.u32 a1, %1, 40;\n add.u32 bl1, %2, %7;\n mov.b64 bd, {bl1, %3};\n tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], bd, %4, t;\n"
-      " add.u32 a1, %1, 48;\n add.u32 bl1, %2, %8;\n mov.b64 bd, {bl1, %3};\n tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], bd, %4, t;\n"
-      " add.u32 a1, %1, 56;\n add.u32 bl1, %2, %9;\n mov.b64 bd, {bl1, %3};\n tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], bd, %4, t;\n"
-      "}\n" ::"r"(d), "r"(a), "r"(bl), "r"(bh), "r"(idesc), "r"(acc), "n"(HALF16), "n"(HALF16 + 2), "n"(HALF16 + 4),
-      "n"(HALF16 + 6)
-      : "memory");
+  if constexpr (PAIR) MOE_TC_MMA_KBLOCK("2");   // M = 256: A rows and B columns from both CTAs of the pair
+  else MOE_TC_MMA_KBLOCK("1");
 }
-
+#undef MOE_TC_MMA_KBLOCK
 __device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t (&v)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
@@ -375,16 +436,29 @@ __device__ __forceinline__ void epilogue_cols(const TcParams &p, const Tile &t, 
   }
 }
 
-template <typename T, int BITS>
+// PAIR: the kernel runs in clusters of two CTAs (CTA pairs, tcgen05 cta_group::2).  A pair tile
+// is 256 output channels x up to 160 rows: each CTA dequantizes its 128 channels into its own
+// tensor memory and copies its half of the tile's rows (rows [n/2 * rank, n/2 * rank + n/2) of
+// the MMA's N = n) into its own shared memory; the rank-0 CTA issues M = 256 MMAs that read both
+// CTAs' operands and commits to both CTAs' barriers.  Each SM then moves half the activation bytes
+// per MMA FLOP through its shared memory.  The rank-1 CTA's dequant groups arrive on its own
+// `ready`; one thread of it (the idle MMA warp's) relays each completed phase to rank 0's
+// `ready`, and its epilogue warps arrive on rank 0's `d_empty`.
+template <typename T, int BITS, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ XMaps maps_x, const __grid_constant__ CUtensorMap map_w,
                    const TcParams p) {
   pdl_enter();   // see launch_pdl
+  static_assert(!PAIR || BITS != 16, "pairs take quantized weights");
   constexpr int kWBytes = WB<BITS>::kBytes;
   constexpr int kWords = WB<BITS>::kWordsPerRow;
   constexpr int kWS = WB<BITS>::kWStages, kBS = WB<BITS>::kBStages;
-  constexpr int kBN = TB<BITS>::kBN, kBHalf = TB<BITS>::kBHalf, kBBytes = TB<BITS>::kBBytes;
+  constexpr int kBN = TB<BITS>::kBN;
+  constexpr int kBRows = PAIR ? kBN / 2 : kBN;          // activation rows a CTA holds per tile
+  constexpr int kBHalf = kBRows * 64 * 2, kBBytes = 2 * kBHalf;
+  constexpr int kBoxUnit = PAIR ? 16 : 32;               // rows of activation box i: kBoxUnit (i + 1)
   constexpr uint32_t kACol0 = TB<BITS>::kACol0;
+  constexpr bool CL = PAIR;                              // waits that see the peer's arrivals
   extern __shared__ __align__(1024) uint8_t dsmem[];
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dsmem) + 1023) & ~uintptr_t(1023));
   uint8_t *sB = base;                                   // kBS x kBBytes (two 1024-aligned K halves)
@@ -405,6 +479,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int E = p.E;
+  // pairs: tiles are dealt per pair; this CTA's 128-channel block of a pair tile by its rank
+  const int prank = PAIR ? int(cluster_rank()) : 0;
+  const int ncbx = PAIR ? p.ncb / 2 : p.ncb;
+  const int tile0 = PAIR ? int(blockIdx.x >> 1) : int(blockIdx.x);
+  const int tstride = PAIR ? int(gridDim.x >> 1) : int(gridDim.x);
+  auto get_tile = [&](int tile) {
+    Tile t = decode_tile(tile, s_tstart, s_off, E, ncbx, kBN);
+    if constexpr (PAIR) t.cb = 2 * t.cb + prank;
+    return t;
+  };
 
   // ---- setup: barriers, TMEM, tile table
   if (tid == 0) {
@@ -412,28 +496,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&wfull[s], 1);
       mbar_init(&wfree[s], 4);   // the dequant group's 4 warps (quantized weights)
       mbar_init(&bfull[s], 1);
-      mbar_init(&ready[s], 4);
+      mbar_init(&ready[s], PAIR && prank == 0 ? 5 : 4);   // + the peer's relayed phase
       mbar_init(&sfree[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&d_full[s], 1);
-      mbar_init(&d_empty[s], kEpiWarps);
+      mbar_init(&d_empty[s], PAIR ? 2 * kEpiWarps : kEpiWarps);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   if (warp == 0) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(su32(tmem_slot)),
-                 "r"(kTmemCols));
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::);
+    if constexpr (PAIR) {   // one warp of each CTA of the pair
+      asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(su32(tmem_slot)),
+                   "r"(kTmemCols));
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;\n" ::);
+    } else {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(su32(tmem_slot)),
+                   "r"(kTmemCols));
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::);
+    }
   }
   int cnt = 0;
   // checked build: unusable offsets leave the kernel without tiles (nothing is read or written)
   const bool off_ok = p.offsets == nullptr || offsets_usable(p.offsets, E, p.R, [] { check_fail(kCheckOffsets); });
   if (tid < E && off_ok) {   // no offsets array: one expert owning all R rows
     const int o0 = p.offsets ? p.offsets[tid] : 0, o1 = p.offsets ? p.offsets[tid + 1] : p.R;
-    cnt = ((o1 - o0 + kBN - 1) / kBN) * p.ncb;
+    cnt = ((o1 - o0 + kBN - 1) / kBN) * ncbx;
     s_off[tid] = o0;
     if (tid == E - 1) s_off[E] = o1;
   }
@@ -441,18 +531,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int total_tiles = block_exclusive_scan(cnt, &start, scratch);  // contains __syncthreads
   if (tid < E) s_tstart[tid] = start;
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR) cluster_sync();   // both CTAs' barriers initialised before any remote arrival
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const uint32_t ready_r0 = PAIR ? map_to_rank(ready, 0) : 0u;     // rank 0's barriers, cluster addresses
+  const uint32_t d_empty_r0 = PAIR ? map_to_rank(d_empty, 0) : 0u;
   const int nkb = p.K / kBK;
   const int is_bf16 = std::is_same<T, __nv_bfloat16>::value ? 1 : 0;
   // the drain of a copy ring: every issued fill has landed before the CTA may exit (2 bits per
   // stage: 0 = never filled, else the parity of its last fill + 1)
-  auto drain_ring = [&](uint64_t *fullb, int nst, uint32_t issued) {
+  // (pairs: also every release of a stage the rank-0 CTA's commits send here has arrived)
+  auto drain_ring = [&](uint64_t *fullb, uint64_t *freeb, int nst, uint32_t issued) {
     for (int s = 0; s < nst; ++s)
       if ((issued >> (2 * s)) & 3u) {
         volatile int never = 0;
         mbar_wait(&fullb[s], ((issued >> (2 * s)) & 3u) - 1, &never, kErrTimeoutDrain);
+        if (freeb != nullptr) mbar_wait<CL>(&freeb[s], ((issued >> (2 * s)) & 3u) - 1, &never, kErrTimeoutDrain);
       }
   };
 
@@ -461,23 +556,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t it = 0, issued = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-        const Tile t = decode_tile(tile, s_tstart, s_off, E, p.ncb, kBN);
+      for (int tile = tile0; ok && tile < total_tiles; tile += tstride) {
+        const Tile t = get_tile(tile);
+        // pairs: the MMA's N columns (rows of the tile) split in halves, this CTA copies its half
+        const int crows = PAIR ? ((t.nrows + 15) & ~15) >> 1 : t.nrows;
+        const int brow = t.row0 + prank * crows;
+        const int nb = (crows + kBoxUnit - 1) / kBoxUnit;   // box units covering the CTA's rows
+        const CUtensorMap *mx = &maps_x.box[nb - 1];
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % kBS;
-          if (!mbar_wait(&sfree[s], ((it / kBS) & 1) ^ 1, abort_flag, kErrTimeoutFree)) {
+          if (!mbar_wait<CL>(&sfree[s], ((it / kBS) & 1) ^ 1, abort_flag, kErrTimeoutFree)) {
             ok = false;
             break;
           }
-          const int nb = (t.nrows + 31) >> 5;            // 32-row units of the tile's box
-          const CUtensorMap *mx = &maps_x.box[nb - 1];
-          mbar_expect_tx(&bfull[s], uint32_t(nb) * 32 * 128 * 2);
-          tma_load_2d(sB + s * kBBytes, mx, kb * kBK, t.row0, &bfull[s]);
-          tma_load_2d(sB + s * kBBytes + kBHalf, mx, kb * kBK + 64, t.row0, &bfull[s]);
+          mbar_expect_tx(&bfull[s], uint32_t(nb) * kBoxUnit * 128 * 2);
+          tma_load_2d(sB + s * kBBytes, mx, kb * kBK, brow, &bfull[s]);
+          tma_load_2d(sB + s * kBBytes + kBHalf, mx, kb * kBK + 64, brow, &bfull[s]);
           issued = (issued & ~(3u << (2 * s))) | ((((it / kBS) & 1) + 1) << (2 * s));
         }
       }
-      drain_ring(bfull, kBS, issued);
+      drain_ring(bfull, PAIR ? sfree : nullptr, kBS, issued);
     }
   } else if (warp == kWProdWarp) {
     // ------------------------------------------------ weight copies (TMA) + L2 prefetch
@@ -485,9 +583,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // rolling L2 prefetch of the weight blocks kPrefetch K blocks ahead of the stage copies (into
       // the CTA's next tile), so a stage copy waits on L2 rather than DRAM
       constexpr int kPrefetch = 8;
-      int pf_tile = blockIdx.x, pf_kb = 0, pf_A = 0, pf_B = 0;
+      int pf_tile = tile0, pf_kb = 0, pf_A = 0, pf_B = 0;
       auto pf_rows = [&]() {
-        const Tile tn = decode_tile(pf_tile, s_tstart, s_off, E, p.ncb, kBN);
+        const Tile tn = get_tile(pf_tile);
         pf_A = tn.e * p.N + (p.swiglu ? tn.cb * (kBM / 2) : tn.cb * kBM);
         pf_B = p.swiglu ? tn.e * p.N + (p.N >> 1) + tn.cb * (kBM / 2) : pf_A + kBM / 2;
       };
@@ -505,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (++pf_kb == nkb) {
           pf_kb = 0;
-          pf_tile += gridDim.x;
+          pf_tile += tstride;
           if (pf_tile < total_tiles) pf_rows();
         }
       };
@@ -513,8 +611,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < kPrefetch; ++i) pf_step();
       uint32_t it = 0, issued = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-        const Tile t = decode_tile(tile, s_tstart, s_off, E, p.ncb, kBN);
+      for (int tile = tile0; ok && tile < total_tiles; tile += tstride) {
+        const Tile t = get_tile(tile);
         const int rowA = t.e * p.N + (p.swiglu ? t.cb * (kBM / 2) : t.cb * kBM);
         const int rowB = p.swiglu ? t.e * p.N + (p.N >> 1) + t.cb * (kBM / 2) : rowA + kBM / 2;
         for (int kb = 0; kb < nkb; ++kb, ++it) {
@@ -538,19 +636,35 @@ __global__ void __launch_bounds__(kThreads, 1)
           pf_step();
         }
       }
-      drain_ring(wfull, kWS, issued);
+      drain_ring(wfull, nullptr, kWS, issued);
+    }
+  } else if (warp == kMmaWarp && PAIR && prank == 1) {
+    // ------------------------------------------------ pairs, rank 1: relay of `ready` to rank 0
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tile = tile0; ok && tile < total_tiles; tile += tstride) {
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = it % kAStages;
+          if (!mbar_wait(&ready[s], (it / kAStages) & 1, abort_flag, kErrTimeoutReady)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_cluster(ready_r0 + uint32_t(s) * 8u);
+        }
+      }
     }
   } else if (warp == kMmaWarp) {
-    // ------------------------------------------------ MMA issuer
+    // ------------------------------------------------ MMA issuer (pairs: rank 0 issues for both CTAs)
     if (lane == 0) {
       uint32_t it = 0, tcount = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x, ++tcount) {
-        const Tile t = decode_tile(tile, s_tstart, s_off, E, p.ncb, kBN);
+      for (int tile = tile0; ok && tile < total_tiles; tile += tstride, ++tcount) {
+        const Tile t = get_tile(tile);
         const int n = (t.nrows + 15) & ~15;
-        const uint32_t idesc = idesc_f16(is_bf16, kBM, n);
+        const uint32_t idesc = idesc_f16(is_bf16, PAIR ? 2 * kBM : kBM, n);
         const int db = tcount & 1;
-        if (!mbar_wait(&d_empty[db], ((tcount >> 1) & 1) ^ 1, abort_flag, kErrTimeoutD)) break;
+        if (!mbar_wait<CL>(&d_empty[db], ((tcount >> 1) & 1) ^ 1, abort_flag, kErrTimeoutD)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + uint32_t(db * kBN);
         for (int kb = 0; kb < nkb; ++kb, ++it) {
@@ -560,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // its A stage is filled and it has seen the block's activation copy land
           if (!(BITS == 16 ? mbar_wait(&wfull[s], par, abort_flag, kErrTimeoutFull) &&
                                  mbar_wait(&bfull[s], par, abort_flag, kErrTimeoutFull)
-                           : mbar_wait(&ready[s], par, abort_flag, kErrTimeoutReady))) {
+                           : mbar_wait<CL>(&ready[s], par, abort_flag, kErrTimeoutReady))) {
             ok = false;
             break;
           }
@@ -577,14 +691,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           } else {
             static_assert(kBK == 128, "tc_mma_kblock_ts issues the eight MMAs of a 128-wide K block");
-            tc_mma_kblock_ts<kBHalf / 16>(d_tmem, tmem + kACol0 + uint32_t(s) * kAStageCols, bd0, idesc, uint32_t(kb));
+            tc_mma_kblock_ts<kBHalf / 16, PAIR>(d_tmem, tmem + kACol0 + uint32_t(s) * kAStageCols, bd0, idesc,
+                                                uint32_t(kb));
           }
-          tc_commit(&sfree[s]);
+          if constexpr (PAIR) tc_commit_pair(&sfree[s]);
+          else tc_commit(&sfree[s]);
         }
-        if (ok) tc_commit(&d_full[db]);
+        if (ok) {
+          if constexpr (PAIR) tc_commit_pair(&d_full[db]);
+          else tc_commit(&d_full[db]);
+        }
       }
-      // drain: all issued MMAs complete before TMEM is released
-      tc_commit(drain);
+      // drain: all issued MMAs complete before TMEM is released (and, with pairs, before the
+      // cluster barrier that lets the other CTA exit)
+      if constexpr (PAIR) tc_commit_pair_local(drain);
+      else tc_commit(drain);
       volatile int never = 0;
       mbar_wait(drain, 0, &never, kErrTimeoutDrain);
     }
@@ -597,8 +718,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int swz = ((r * WB<BITS>::kRowBytes) >> 7) & WB<BITS>::kSwzMask;   // this row's piece swizzle
     uint32_t it = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-      const Tile t = decode_tile(tile, s_tstart, s_off, E, p.ncb, kBN);
+    for (int tile = tile0; ok && tile < total_tiles; tile += tstride) {
+      const Tile t = get_tile(tile);
       int ch;
       if (p.swiglu) ch = r < kBM / 2 ? t.cb * (kBM / 2) + r : (p.N >> 1) + t.cb * (kBM / 2) + (r - kBM / 2);
       else ch = t.cb * kBM + r;
@@ -614,7 +735,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // the block's weights have landed, and the MMAs that read this A stage last are done
         if (!mbar_wait(&wfull[sw], (it / kWS) & 1, abort_flag, kErrTimeoutFull) ||
-            !mbar_wait(&sfree[sa], ((it / kAStages) & 1) ^ 1, abort_flag, kErrTimeoutFree)) {
+            !mbar_wait<CL>(&sfree[sa], ((it / kAStages) & 1) ^ 1, abort_flag, kErrTimeoutFree)) {
           ok = false;
           break;
         }
@@ -673,10 +794,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;
     const int half = warp >> 2;   // tile columns: 32-wide chunks 2 c + half
     uint32_t tcount = 0;
-    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++tcount) {
-      const Tile t = decode_tile(tile, s_tstart, s_off, E, p.ncb, kBN);
+    for (int tile = tile0; tile < total_tiles; tile += tstride, ++tcount) {
+      const Tile t = get_tile(tile);
       const int db = tcount & 1;
-      if (!mbar_wait(&d_full[db], (tcount >> 1) & 1, abort_flag, kErrTimeoutD)) break;
+      if (!mbar_wait<CL>(&d_full[db], (tcount >> 1) & 1, abort_flag, kErrTimeoutD)) break;
       tc_fence_after();
       const int c_lo = 32 * half, c_hi = t.nrows;
       const uint32_t tmem_d = tmem + uint32_t(db * kBN);
@@ -688,16 +809,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&d_empty[db]);
+      if (lane == 0) {
+        if constexpr (PAIR) mbar_arrive_cluster(d_empty_r0 + uint32_t(db) * 8u);   // rank 0 issues the MMAs
+        else mbar_arrive(&d_empty[db]);
+      }
     }
   }
 
-  // ---- teardown: everyone done, release tensor memory
+  // ---- teardown: everyone done (pairs: in both CTAs), release tensor memory
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR) cluster_sync();
+  else __syncthreads();
   tc_fence_after();
-  if (warp == 0)
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kTmemCols));
+  if (warp == 0) {
+    if constexpr (PAIR)
+      asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kTmemCols));
+    else
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kTmemCols));
+  }
 }
 
 // ---------------------------------------------------------------- host side
@@ -720,11 +849,11 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-size_t smem_bytes(int bits) {
+size_t smem_bytes(int bits, bool pair) {
   const size_t wbytes = bits == 4 ? WB<4>::kBytes : (bits == 8 ? WB<8>::kBytes : WB<16>::kBytes);
   const int ws = bits == 4 ? WB<4>::kWStages : (bits == 8 ? WB<8>::kWStages : WB<16>::kWStages);
   const int bs = bits == 4 ? WB<4>::kBStages : (bits == 8 ? WB<8>::kBStages : WB<16>::kBStages);
-  const size_t bbytes = bits == 16 ? TB<16>::kBBytes : TB<4>::kBBytes;
+  const size_t bbytes = (bits == 16 ? TB<16>::kBBytes : TB<4>::kBBytes) / (pair ? 2 : 1);
   return 1024 /*align slack*/ + bs * bbytes + ws * wbytes + 2 * 32 * 64 * 4 + (2 * ws + 2 * bs + 2 * kAStages + 5) * 8 +
          (2 * (kMaxE + 1) + 32 + 2) * 4;
 }
@@ -741,16 +870,46 @@ static_assert(1024 + WB<16>::kBStages * TB<16>::kBBytes + WB<16>::kWStages * WB<
                   232448,
               "16-bit shared memory");
 
-template <typename T, int BITS>
-int launch_typed(const GemmArgs &g, cudaStream_t st) {
+// Pairs the device can run at once (0 if the pair kernel cannot be placed), per instance and
+// device; also sets the pair kernel's shared-memory opt-in, which the query needs.
+template <typename T, int BITS> int max_pairs(size_t smem, int dev) {
+  static std::atomic<int> c[64];   // 0 = not asked yet, else pairs + 1
+  int v = c[dev].load(std::memory_order_relaxed);
+  if (v == 0) {
+    v = 1;
+    if (cudaFuncSetAttribute(gemm_tc_kernel<T, BITS, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) ==
+        cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.gridDim = dim3(2 * unsigned(num_sms()));
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = smem;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<T, BITS, true>, &cfg) == cudaSuccess) v = n + 1;
+    }
+    cudaGetLastError();   // a refused query leaves no error behind: the single-CTA kernel runs
+    c[dev].store(v, std::memory_order_relaxed);
+  }
+  return v - 1;
+}
+
+template <typename T, int BITS, bool PAIR>
+int launch_typed(const GemmArgs &g, cudaStream_t st, int dev, int pairs_max) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return set_error(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   XMaps mx{};
   CUtensorMap mw;
-  for (int i = 0; i < TB<BITS>::kBN / 32; ++i) {   // box i: 64 columns (one 128-byte swizzle atom) x 32 (i + 1) rows
+  constexpr int kUnit = PAIR ? 16 : 32;   // box heights: a CTA's rows of a tile, in these units
+  for (int i = 0; i < TB<BITS>::kBN / 32; ++i) {   // box i: 64 columns (one 128-byte swizzle atom) x kUnit (i + 1) rows
     const cuuint64_t dims[2] = {cuuint64_t(g.K), cuuint64_t(g.R)};
     const cuuint64_t strides[1] = {cuuint64_t(g.K) * 2};
-    const cuuint32_t box[2] = {64u, cuuint32_t(32 * (i + 1))};
+    const cuuint32_t box[2] = {64u, cuuint32_t(kUnit * (i + 1))};
     const cuuint32_t es[2] = {1, 1};
     const CUresult r = enc(&mx.box[i], std::is_same<T, __half>::value ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                            2, const_cast<void *>(g.a), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -794,24 +953,57 @@ int launch_typed(const GemmArgs &g, cudaStream_t st) {
   tp.out_dtype = g.out_dtype;
   tp.swiglu = g.act == MOE_ACT_SWIGLU ? 1 : 0;
   tp.ncb = g.N / kBM;  // SwiGLU: 64 gate + 64 up channels per 128-channel block, the same count
-  const size_t smem = smem_bytes(BITS);
-  // the shared-memory opt-in is a per-device attribute of the kernel: set once per device
-  static std::atomic<bool> attr_set[64];   // one per instance (template) and device
+  const size_t smem = smem_bytes(BITS, PAIR);
+  // tiles upper bound: (row tiles) x channel blocks (pairs: x channel-block pairs)
+  const int64_t row_tiles = std::min<int64_t>(g.E, g.R) + cdiv(g.R, TB<BITS>::kBN);
+  if constexpr (PAIR) {   // the opt-in was set by max_pairs
+    const int64_t tiles = row_tiles * (tp.ncb / 2);
+    const int pairs = int(std::max<int64_t>(1, std::min<int64_t>(tiles, pairs_max)));
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(2 * unsigned(pairs));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    cudaLaunchKernelEx(&cfg, gemm_tc_kernel<T, BITS, true>, mx, mw, tp);
+    return check_launch("grouped_gemm_tc (pairs)");
+  } else {
+    // the shared-memory opt-in is a per-device attribute of the kernel: set once per device
+    static std::atomic<bool> attr_set[64];   // one per instance (template) and device
+    if (!attr_set[dev].load(std::memory_order_relaxed)) {
+      if (cudaFuncSetAttribute(gemm_tc_kernel<T, BITS, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               int(smem)) != cudaSuccess)
+        return check_launch("gemm_tc attribute");
+      attr_set[dev].store(true, std::memory_order_relaxed);
+    }
+    const int64_t tiles = row_tiles * tp.ncb;
+    const int grid = int(std::max<int64_t>(1, std::min<int64_t>(tiles, num_sms())));
+    launch_pdl(gemm_tc_kernel<T, BITS, false>, dim3(grid), dim3(kThreads), smem, st, mx, mw, tp);
+    return check_launch("grouped_gemm_tc");
+  }
+}
+
+// Pairs take 4- and 8-bit weights whose channel blocks come in pairs, on devices that can place
+// them; everything else runs on single CTAs.
+template <typename T, int BITS> int launch_tc(const GemmArgs &g, cudaStream_t st) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return check_launch("gemm_tc: cudaGetDevice");
   if (dev < 0 || dev >= 64) return set_error(MOE_ERR_UNSUPPORTED, "gemm_tc: device index %d >= 64", dev);
-  if (!attr_set[dev].load(std::memory_order_relaxed)) {
-    if (cudaFuncSetAttribute(gemm_tc_kernel<T, BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
-        cudaSuccess)
-      return check_launch("gemm_tc attribute");
-    attr_set[dev].store(true, std::memory_order_relaxed);
+  if constexpr (BITS != 16) {
+    if (g_tc_pairs && (g.N / kBM) % 2 == 0) {
+      const int pm = max_pairs<T, BITS>(smem_bytes(BITS, true), dev);
+      if (pm > 0) return launch_typed<T, BITS, true>(g, st, dev, pm);
+    }
   }
-  // tiles upper bound: (row tiles) x channel blocks
-  const int64_t row_tiles = std::min<int64_t>(g.E, g.R) + cdiv(g.R, TB<BITS>::kBN);
-  const int64_t tiles = row_tiles * tp.ncb;
-  const int grid = int(std::max<int64_t>(1, std::min<int64_t>(tiles, num_sms())));
-  launch_pdl(gemm_tc_kernel<T, BITS>, dim3(grid), dim3(kThreads), smem, st, mx, mw, tp);
-  return check_launch("grouped_gemm_tc");
+  return launch_typed<T, BITS, false>(g, st, dev, 0);
 }
 
 }  // namespace
@@ -836,9 +1028,9 @@ bool tc_supported(const GemmArgs &g) {
 int launch_gemm_tc(const GemmArgs &g, cudaStream_t st) {
   if (g.R == 0) return MOE_OK;
   const bool bf = g.a_dtype == MOE_BF16;
-  if (g.bits == 4) return bf ? launch_typed<__nv_bfloat16, 4>(g, st) : launch_typed<__half, 4>(g, st);
-  if (g.bits == 8) return bf ? launch_typed<__nv_bfloat16, 8>(g, st) : launch_typed<__half, 8>(g, st);
-  return bf ? launch_typed<__nv_bfloat16, 16>(g, st) : launch_typed<__half, 16>(g, st);
+  if (g.bits == 4) return bf ? launch_tc<__nv_bfloat16, 4>(g, st) : launch_tc<__half, 4>(g, st);
+  if (g.bits == 8) return bf ? launch_tc<__nv_bfloat16, 8>(g, st) : launch_tc<__half, 8>(g, st);
+  return bf ? launch_tc<__nv_bfloat16, 16>(g, st) : launch_tc<__half, 16>(g, st);
 }
 
 int read_device_error(cudaStream_t st, int *out) {

@@ -149,6 +149,8 @@ bool tc_supported(const GemmArgs &g);
 // Shapes the tcgen05 kernel takes (the launch also needs an offsets array).
 bool tc_shape_ok(int64_t E, int64_t K, int64_t N, int bits, int group, int act);
 int launch_gemm_tc(const GemmArgs &g, cudaStream_t st);
+// CTA pairs for the quantized tcgen05 GEMM (moe_set_gemm_pairs): returns the previous setting
+int set_gemm_pairs(int on);
 int read_device_error(cudaStream_t st, int *out);
 int decode_error_take(int *out);   // device error word of the one-launch decode layer
 

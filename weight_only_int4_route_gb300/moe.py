@@ -55,6 +55,7 @@ _SIGS = {
     "moe_device_error": (_c_int, [_vp, ctypes.POINTER(ctypes.c_int32)]),
     "moe_checked_build": (_c_int, []),
     "moe_set_decode_mode": (_c_int, [_c_int]),
+    "moe_set_gemm_pairs": (_c_int, [_c_int]),
     "moe_check_status": (_c_int, [_vp, ctypes.POINTER(ctypes.c_int32)]),
     "moe_packed_size": (_c_size, [_c_i64, _c_i64, _c_i64, _c_int, _c_int]),
     "moe_packed_scale_offset": (_c_size, [_c_i64, _c_i64, _c_i64, _c_int]),
@@ -141,6 +142,15 @@ def set_decode_mode(mode: str) -> str:
     if prev < 0:
         _check(prev, "moe_set_decode_mode")
     return {v: k for k, v in _DECODE_MODES.items()}[prev]
+
+
+def set_gemm_pairs(on: bool) -> bool:
+    """CTA pairs (M = 256) for the quantized tcgen05 GEMM on or off (process-wide); returns the
+    previous setting."""
+    prev = lib().moe_set_gemm_pairs(1 if on else 0)
+    if prev < 0:
+        _check(prev, "moe_set_gemm_pairs")
+    return bool(prev)
 
 
 def check_status(device="cuda:0", L: Optional[ctypes.CDLL] = None) -> tuple[int, int]:
