@@ -453,6 +453,7 @@ template <typename T> Inst pick_t(int bits, int nt, int mt, bool grouped) {
   if (bits == B && nt == N_ && mt == M_ && grouped == G_)                \
     return Inst{kernel_of<T, B, N_, M_, G_>(), smem_of<B, N_, M_>()};
   MOE_GV(4, 1, 2, true) MOE_GV(4, 2, 2, true) MOE_GV(4, 1, 2, false) MOE_GV(4, 2, 2, false)
+  MOE_GV(4, 1, 4, true) MOE_GV(4, 2, 4, true) MOE_GV(4, 1, 4, false) MOE_GV(4, 2, 4, false)
   MOE_GV(8, 1, 2, true) MOE_GV(8, 2, 2, true) MOE_GV(8, 1, 2, false) MOE_GV(8, 2, 2, false)
   MOE_GV(16, 1, 1, false) MOE_GV(16, 2, 1, false)
 #undef MOE_GV
@@ -466,8 +467,8 @@ Inst pick(bool bf, int bits, int nt, int mt, bool grouped) {
 // attribute of the kernel, is set on the way); computed once per instance and device.
 int blocks_per_sm(bool bf, int bits, int nt, int mt, bool grouped) {
   static std::mutex mu;
-  static int cache[64][2][3][2][2][2] = {};
-  if (nt < 1 || nt > 2 || mt < 1 || mt > 2) return 1;
+  static int cache[64][2][3][2][4][2] = {};
+  if (nt < 1 || nt > 2 || mt < 1 || mt > 4) return 1;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
     cudaGetLastError();   // the launch then reports the problem
@@ -505,41 +506,59 @@ bool gemv_shape_ok(int64_t K, int64_t N, int bits, int act) {
 // chunks is estimated (experts drawn uniformly); the split S (a divisor of K/128) minimizes the
 // bytes the busiest warp streams, counting the fp32 partial slices a split writes and re-reads.
 GemmPlan plan_gemv(int64_t R, int64_t E, int64_t K, int64_t N, int bits, int act, bool want_partial) {
-  GemmPlan pl{};
-  pl.kind = kKindGemv;
   const double er = double(std::max<int64_t>(E, 1));
   const double active = std::max(1.0, er * (1.0 - std::pow(1.0 - 1.0 / er, double(std::max<int64_t>(R, 1)))));
   const double avg = double(std::max<int64_t>(R, 1)) / active;
-  pl.nt = avg <= 8.0 ? 1 : 2;
+  const int nt = avg <= 8.0 ? 1 : 2;
   const int64_t m16 = act == MOE_ACT_SWIGLU ? (N / 2) / 8 : N / 16;   // 16-channel m-tiles
-  pl.mt = bits != 16 ? 2 : 1;   // 16-bit weights: one m-tile keeps the ring small
-  pl.ng = int(m16 / pl.mt);
   const int64_t nck = K / 128;
   // row chunks: one ragged tail per active expert on average, never more than the rows allow
-  const double rc = std::min(std::ceil(active + 0.5 * double(R) / (8.0 * pl.nt)),
-                             active - 1.0 + std::ceil(double(R) / (8.0 * pl.nt)));
-  const int64_t warps = int64_t(num_sms()) * blocks_per_sm(false, bits, pl.nt, pl.mt, bits != 16) * kWarps;
-  const double step_bytes = double(pl.mt) * 16 * 128 * bits / 8;   // weight bytes per warp per chunk
+  const double rc = std::min(std::ceil(active + 0.5 * double(R) / (8.0 * nt)),
+                             active - 1.0 + std::ceil(double(R) / (8.0 * nt)));
   const size_t kPartialCap = size_t(256) << 20;
-  double best = 0;
-  int64_t S = 1;
-  for (int64_t s = 1; s <= nck; ++s) {
-    if (nck % s) continue;
-    if (s > 1 && size_t(s) * size_t(R) * size_t(N) * 4 > kPartialCap) break;
-    const double units = rc * double(pl.ng) * double(s);
-    const double per = std::ceil(units / double(warps));
-    double cost = per * double(nck / s) * step_bytes;
-    if (want_partial || s > 1) cost += 2.0 * double(s) * double(R) * double(N) * 4 / double(warps);
-    if (s == 1 || cost < best * 0.98) {
-      best = cost;
-      S = s;
+  // For one m16 tile count per unit (mt): the K split with the least per-warp byte load (units
+  // dealt round-robin over the resident warps); *steps = the 128-wide chunks a warp streams.
+  auto plan_for = [&](int mt, double *steps) {
+    GemmPlan pl{};
+    pl.kind = kKindGemv;
+    pl.nt = nt;
+    pl.mt = mt;
+    pl.ng = int(m16 / mt);
+    const int wps = blocks_per_sm(false, bits, nt, mt, bits != 16) * kWarps;
+    const int64_t warps = int64_t(num_sms()) * wps;
+    const double step_bytes = double(mt) * 16 * 128 * bits / 8;   // weight bytes per warp per chunk
+    double best = 0, best_per = 1;
+    int64_t S = 1;
+    for (int64_t s = 1; s <= nck; ++s) {
+      if (nck % s) continue;
+      if (s > 1 && size_t(s) * size_t(R) * size_t(N) * 4 > kPartialCap) break;
+      const double units = rc * double(pl.ng) * double(s);
+      const double per = std::ceil(units / double(warps));
+      double cost = per * double(nck / s) * step_bytes;
+      if (want_partial || s > 1) cost += 2.0 * double(s) * double(R) * double(N) * 4 / double(warps);
+      if (s == 1 || cost < best * 0.98) {
+        best = cost;
+        best_per = per;
+        S = s;
+      }
     }
-  }
-  pl.splits = int(S);
-  pl.ks = int(nck / S) * 128;
-  pl.ch = int(nck / S);
-  pl.partial = want_partial || S > 1;
-  return pl;
+    pl.splits = int(S);
+    pl.ks = int(nck / S) * 128;
+    pl.ch = int(nck / S);
+    pl.partial = want_partial || S > 1;
+    *steps = best_per * double(pl.ch);
+    return pl;
+  };
+  double st2 = 0, st4 = 0;
+  if (bits == 16) return plan_for(1, &st2);   // 16-bit weights: one m-tile keeps the ring small
+  const GemmPlan p2 = plan_for(2, &st2);
+  if (bits != 4 || m16 % 4 != 0) return p2;
+  // 4 m16 tiles per unit carry twice the weight bytes per ring slot for the same activation slice
+  // (half the warps per SM, each with twice the bytes in flight): measured on GB300 4-8 % faster
+  // where each warp streams a long run of chunks (Phi-shaped decode GEMMs), up to 17 % slower
+  // where it streams a few (Qwen-shaped T = 8 FC1, 16 chunks), so it takes the long runs
+  const GemmPlan p4 = plan_for(4, &st4);
+  return st4 >= 32 ? p4 : p2;
 }
 
 int launch_gemv(const GemmArgs &g, const GemmPlan &pl, cudaStream_t st) {
