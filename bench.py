@@ -414,6 +414,12 @@ MEASURED_TRAFFIC = {
     ("phi", 8192, "fc1"): 567_240_704 + 197_445_632,
     ("encdec_int4", 3840, "fc1"): 75_360_256 + 5_082_624,
     ("encdec_int4", 3840, "fc2"): 98_776_064 + 3_428_864,
+    # decode weight stream (gemv_kernel): several tokens on a graph replay, one token on the
+    # graph-creation call (one token's routing always touches k experts)
+    ("phi", 16, "fc1"): 351_766_784 + 8_243_712,
+    ("phi", 1, "fc1"): 54_117_888 + 119_296,
+    ("qwen", 8, "fc1"): 71_535_616 + 1_062_912,
+    ("dsv2", 32, "fc1"): 84_102_912 + 2_102_784,
 }
 
 
