@@ -289,6 +289,9 @@ typedef struct {
   int32_t *inv_perm; /* (T*k) */
 } moe_layer_routing;
 
+/* Bytes of a layer workspace that serves every moe_layer_forward call of at most T tokens (the
+ * largest requirement over T' <= T: a smaller batch can need more, its split-K plans writing
+ * partial sums in more slices). */
 size_t moe_layer_workspace_size(const moe_layer_desc *desc, int64_t T);
 int moe_layer_routing_view(const moe_layer_desc *desc, int64_t T, void *workspace,
                            moe_layer_routing *view);

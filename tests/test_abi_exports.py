@@ -102,3 +102,16 @@ def test_layer_workspace_query(L):
     bad = M.layer_desc(synth.CONFIGS["tiny"])
     bad.k = 99
     assert L.moe_layer_workspace_size(ctypes.byref(bad), 16) == 0
+
+
+def test_layer_workspace_size_serves_every_smaller_batch(L):
+    """moe_layer_workspace_size(desc, T) is the largest requirement over T' <= T (a smaller batch
+    can need more: its split-K plans write partial sums in more slices), so it never decreases
+    in T and a workspace sized for T serves every call with fewer tokens."""
+    from weight_only_int4_route_gb300 import synth
+    for name, cfg in synth.CONFIGS.items():
+        d = M.layer_desc(cfg)
+        sizes = [L.moe_layer_workspace_size(ctypes.byref(d), T) for T in range(1, 257)]
+        assert all(s > 0 for s in sizes), name
+        assert all(b >= a for a, b in zip(sizes, sizes[1:])), name
+        assert L.moe_layer_workspace_size(ctypes.byref(d), 4096) >= sizes[-1], name

@@ -174,8 +174,8 @@ LayerPlan plan_layer(const moe_layer_desc *d, int64_t T, bool for_size = false) 
     p.o_ys = take(size_t(p.sh2.splits) * T * d->d * 4);
   }
   // the one-launch decode layer's own region, last in the workspace.  For a size query it is the
-  // largest any T' <= min(T, 32) needs, so a workspace sized for T serves every smaller call
-  // (the regions before it only grow with T).
+  // largest any T' <= min(T, 32) needs (moe_layer_workspace_size then takes the largest total
+  // over every T' <= T).
   p.dec = plan_decode(d, std::min<int64_t>(T, 32), decode_warps());
   if (p.dec.ok) {
     size_t bytes = p.dec.bytes;
@@ -385,7 +385,12 @@ extern "C" int moe_shared_expert(const void *x, int x_dtype, const void *w_gate_
 
 extern "C" size_t moe_layer_workspace_size(const moe_layer_desc *desc, int64_t T) {
   if (check_desc(desc) != MOE_OK || T < 0) return 0;
-  return plan_layer(desc, T, true).total;
+  // A smaller batch can need more than a larger one (its split-K GEMM plans write partial sums
+  // in more slices), so the size is the largest requirement over every T' <= T: a workspace of
+  // this size serves every call with at most T tokens.  A plan costs a few microseconds.
+  size_t best = plan_layer(desc, T, true).total;
+  for (int64_t t = 1; t < T; ++t) best = std::max(best, plan_layer(desc, t, true).total);
+  return best;
 }
 
 extern "C" int moe_layer_routing_view(const moe_layer_desc *desc, int64_t T, void *workspace,
