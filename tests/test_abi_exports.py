@@ -115,3 +115,23 @@ def test_layer_workspace_size_serves_every_smaller_batch(L):
         assert all(s > 0 for s in sizes), name
         assert all(b >= a for a, b in zip(sizes, sizes[1:])), name
         assert L.moe_layer_workspace_size(ctypes.byref(d), 4096) >= sizes[-1], name
+
+
+@pytest.mark.parametrize("R,E,K,N,bits,group,act,path", [
+    (64, 8, 1024, 2048, 4, 0, "none", "gemv"),          # 8 rows per expert
+    (128, 8, 1024, 2048, 4, 0, "none", "gemv"),         # 16: the last decode-stream size
+    (136, 8, 1024, 2048, 4, 0, "none", "tcgen05"),      # 17: tensor memory from here
+    (10, 100, 1024, 2048, 4, 0, "none", "gemv"),        # fewer rows than experts: 1 per active expert
+    (136, 8, 1024, 192, 4, 0, "none", "mma"),           # N % 128 != 0: the warp-MMA tile kernel
+    (4000, 8, 1000, 2048, 4, 0, "none", "mma"),         # K % 128 != 0
+    (136, 8, 1024, 2816, 4, 128, "swiglu", "tcgen05"),  # SWIGLU: (N/2) % 64 == 0 suffices
+    (4000, 8, 1024, 2048, 8, 128, "gelu", "tcgen05"),
+    (16, 8, 1024, 2048, 16, 0, "none", "gemv"),         # 16-bit weights: the same thresholds
+    (17, 1, 2048, 11264, 16, 0, "swiglu", "tcgen05"),
+])
+def test_gemm_path_follows_the_documented_rule(L, R, E, K, N, bits, group, act, path):
+    """moe_gemm_path: a = ceil(R / min(E, R)) rows per active expert; a <= 16 the decode
+    weight-stream kernel, a >= 17 the tcgen05 kernel where K % 128 == 0 and N % 128 == 0 (SWIGLU:
+    (N/2) % 64 == 0), else the warp-MMA kernel.  Host-side planning only."""
+    assert M.gemm_path(R, E, K, N, bits, group, act) == path
+
