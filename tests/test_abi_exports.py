@@ -115,6 +115,8 @@ def test_layer_workspace_size_serves_every_smaller_batch(L):
         assert all(s > 0 for s in sizes), name
         assert all(b >= a for a, b in zip(sizes, sizes[1:])), name
         assert L.moe_layer_workspace_size(ctypes.byref(d), 4096) >= sizes[-1], name
+        big = [L.moe_layer_workspace_size(ctypes.byref(d), T) for T in (65535, 65536, 65537, 200000)]
+        assert all(b >= a for a, b in zip(big, big[1:])), name
 
 
 @pytest.mark.parametrize("R,E,K,N,bits,group,act,path", [

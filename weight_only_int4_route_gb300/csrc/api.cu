@@ -387,9 +387,13 @@ extern "C" size_t moe_layer_workspace_size(const moe_layer_desc *desc, int64_t T
   if (check_desc(desc) != MOE_OK || T < 0) return 0;
   // A smaller batch can need more than a larger one (its split-K GEMM plans write partial sums
   // in more slices), so the size is the largest requirement over every T' <= T: a workspace of
-  // this size serves every call with at most T tokens.  A plan costs a few microseconds.
+  // this size serves every call with at most T tokens.  A plan costs a few microseconds.  Split
+  // plans exist only while the rows give fewer tiles than two waves of CTAs (under 64 rows per
+  // CTA of 2 x 256 SMs, 32768 rows) or at most 16 rows per expert (4096 rows): from 65536 tokens
+  // on every plan is unsplit and every region grows with T, so the scan stops there.
   size_t best = plan_layer(desc, T, true).total;
-  for (int64_t t = 1; t < T; ++t) best = std::max(best, plan_layer(desc, t, true).total);
+  const int64_t scan = std::min<int64_t>(T - 1, 65536);
+  for (int64_t t = 1; t <= scan; ++t) best = std::max(best, plan_layer(desc, t, true).total);
   return best;
 }
 
